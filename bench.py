@@ -1,0 +1,372 @@
+"""Throughput of the fused top-K forward-KL loss (forward + backward) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--chunk C]
+                    [--impl fused|reference] [--no-cpu-baseline] [--no-e2e]
+
+One step = fkl_forward + fkl_backward over one batch of synthetic tokens of the
+chosen workload (default: the gpt-oss-20b-like long-context loss, N=32768,
+d=2880, V=201088, K=100, T=1).  Inputs are resident in HBM before the timed
+region; W (1.16 GB) alone is larger than L2, so no flush is needed.  Under
+torchrun (N > 1) every rank runs an independent replica of the same workload on
+its own GPU: the loss has no exchange step on one GPU per problem, so the job's
+value is the tokens of all ranks over the slowest rank's time.
+
+`--impl reference` times the fp64 CPU oracle instead, on a bounded row sample
+of the same workload per step (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused top-K KL fwd+bwd tokens/s at V=201088; % of bf16 tensor peak; peak GB"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the
+# kernel source digest they were taken on (see profiles/); stale digests give null.
+TRAFFIC = {}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_digest():
+    m = hashlib.sha256()
+    for f in ("gemm_tc.cu", "ptx.cuh", "fkl_internal.h"):
+        with open(os.path.join(ROOT, "lm_head_kl_fkl_b300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:12]
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def threads_used():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def oracle_step_on_sample(x, rows, Wf):
+    """One oracle forward + backward over a row sample (the oracle as it stands)."""
+    import oracle
+    from lm_head_kl_fkl_b300 import synth
+    hs = synth.bf16_bits_to_f64(x["h"][rows])
+    f = oracle.forward(hs, Wf, x["idx"][rows], x["t"][rows], x["mask"][rows], x["T"])
+    g = oracle.backward(hs, Wf, x["idx"][rows], x["t"][rows], x["mask"][rows], x["T"])
+    return f, g
+
+
+def cpu_baseline(x, budget_s=12.0, max_rows=1024):
+    """Oracle tokens/s on a bounded sample of the workload's rows (fp64, host cores)."""
+    from lm_head_kl_fkl_b300 import synth
+    Wf = synth.bf16_bits_to_f64(x["W"])
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(x["N"], 8, replace=False))
+    t0 = time.perf_counter()
+    oracle_step_on_sample(x, rows, Wf)
+    per_row = (time.perf_counter() - t0) / len(rows)
+    n = int(min(max_rows, max(8, budget_s / max(per_row, 1e-6))))
+    rows = np.sort(rng.choice(x["N"], n, replace=False))
+    t0 = time.perf_counter()
+    oracle_step_on_sample(x, rows, Wf)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": threads_used(), "kind": "oracle",
+            "sample": f"{n} seeded rows of the {x['name']} workload (full d and V), fp64 forward + "
+                      f"backward, {dt:.1f} s"}
+
+
+def workload(cfg):
+    from lm_head_kl_fkl_b300 import synth
+    x = synth.config_inputs(cfg)
+    c = synth.CONFIGS[cfg]
+    return x, c
+
+
+def config_dict(c, chunk, world):
+    return {"workload": f"{c.name} fused top-K KL loss", "N": c.N, "d": c.d, "V": c.V, "K": c.K,
+            "T": c.T, "pad_frac": c.pad_frac, "teacher_ids": c.index, "chunk": chunk or "default",
+            "global_batch": c.N * world, "l2": "no flush: W (bf16 V x d) alone exceeds the 126 MB L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    x, c = workload(args.config)
+    from lm_head_kl_fkl_b300 import synth
+    Wf = synth.bf16_bits_to_f64(x["W"])
+    rng = np.random.default_rng(2)
+    n = args.ref_rows
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(x["N"], n, replace=False))
+        t0 = time.perf_counter()
+        oracle_step_on_sample(x, rows, Wf)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = n / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(c, args.chunk, 1),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads_used(),
+                             "kind": "oracle",
+                             "sample": f"{n} seeded rows per step of the {c.name} workload, fp64"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_fused(args):
+    import torch
+    import torch.distributed as dist
+    from lm_head_kl_fkl_b300 import api
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    x, c = workload(args.config)
+    N, d, V, K, T = c.N, c.d, c.V, c.K, c.T
+    stream = torch.cuda.current_stream(dev)
+
+    def dev_tensor(a, dtype=None):
+        t = torch.from_numpy(a)
+        return (t.view(dtype) if dtype is not None else t).to(dev)
+
+    h = dev_tensor(x["h"].view(np.int16), torch.bfloat16)
+    W = dev_tensor(x["W"].view(np.int16), torch.bfloat16)
+    idx, t, mask = dev_tensor(x["idx"]), dev_tensor(x["t"]), dev_tensor(x["mask"])
+    ws = api.alloc_workspace(N, d, V, K, args.chunk, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dh = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    base_mem = torch.cuda.memory_allocated(dev)
+
+    def step():
+        api.forward(h, W, idx, t, mask, T, args.chunk, ws=ws, loss=loss, lse=lse)
+        api.backward(h, W, idx, t, mask, T, lse, chunk=args.chunk, ws=ws, dh=dh, dW=dW)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if api.get_status(ws) != 0:
+        raise RuntimeError(f"device status {api.get_status(ws)} after warm-up")
+
+    # ---- timed region: device-resident inputs
+    api.profile_reset()
+    api.profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = api.launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    api.profile_enable(False)
+    launches = api.launch_count() - launches0
+    ms = ev0.elapsed_time(ev1)
+    prof = api.profile_read()
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    peak_mem = torch.cuda.max_memory_allocated(dev)
+    status = api.get_status(ws)
+    ms_per_step = ms / args.steps
+    tokens = N * world * args.steps
+    value = tokens / (ms / 1e3)
+    flop_step = 8.0 * N * d * V
+    tflops = flop_step / (ms_per_step / 1e3) / 1e12
+
+    peaks, peaks_kind = load_peaks()
+    gemms = {k: v for k, v in prof.items() if v[2] > 0}
+    dom = max(gemms, key=lambda k: gemms[k][0]) if gemms else None
+    roofline = None
+    if dom:
+        tot_ms, n_l, fl = gemms[dom]
+        achieved = fl / (tot_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        dig = kernel_digest()
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak, "traffic": TRAFFIC.get((dom, dig)),
+                    "peak_kind": f"bf16 dense, sustained, {peaks_kind}",
+                    "flop_per_launch": fl / n_l, "launch_ms": tot_ms / n_l, "launches": n_l}
+    kernels = {k: {"ms_total": v[0], "launches": v[1], "share": v[0] / max(1e-9, sum(p[0] for p in prof.values())),
+                   **({"tflops": v[2] / (v[0] / 1e3) / 1e12} if v[2] > 0 else {})}
+               for k, v in prof.items()}
+
+    # ---- e2e: the public API with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hp = torch.from_numpy(x["h"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        ip, tp, mp = (torch.from_numpy(x[k]).pin_memory() for k in ("idx", "t", "mask"))
+        lossp = torch.empty(1, dtype=torch.float32).pin_memory()
+        h_in, idx_in, t_in, m_in = (torch.empty_like(a, device=dev) for a in (hp, ip, tp, mp))
+
+        def e2e_step():
+            h_in.copy_(hp, non_blocking=True)
+            idx_in.copy_(ip, non_blocking=True)
+            t_in.copy_(tp, non_blocking=True)
+            m_in.copy_(mp, non_blocking=True)
+            api.forward(h_in, W, idx_in, t_in, m_in, T, args.chunk, ws=ws, loss=loss, lse=lse)
+            api.backward(h_in, W, idx_in, t_in, m_in, T, lse, chunk=args.chunk, ws=ws, dh=dh, dW=dW)
+            lossp.copy_(loss, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+            stream.synchronize()  # the loss is read on the host every step
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ems], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        bi = sum(a.numel() * a.element_size() for a in (hp, ip, tp, mp))
+        e2e = {"value": tokens / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": 4, "ms_per_step": ems / args.steps,
+               "resident": "W (model weight) stays on the device; h, teacher ids/logits and mask are copied per step"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": config_dict(c, args.chunk, world),
+                "tflops": tflops,
+                "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
+                                      "sustained": tflops / peaks["bf16_tflops_sustained"],
+                                      "kind": peaks_kind},
+                "peak_mem_gb": peak_mem / 1e9,
+                "workspace_gb": ws.numel() / 1e9,
+                "resident_gb": base_mem / 1e9,
+                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clk.summary(), "gpu_launches": launches, "device_status": status,
+                "kernel_digest": kernel_digest()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0 if status == 0 else 1
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--impl", choices=["fused", "reference"], default="fused")
+    ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "fused":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_fused(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

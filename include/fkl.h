@@ -1,0 +1,133 @@
+/*
+ * fkl.h -- C ABI of libfkl.so: the fused chunked top-K forward-KL distillation
+ * loss over an LM head, on one B300 (sm_103a).
+ *
+ * The operation.  Student hidden states h[N,d] (bf16) meet the LM-head weight
+ * W[V,d] (bf16); z = h W^T is formed tile by tile on the tensor cores and never
+ * stored.  Each token carries an offline teacher cache of K (index, logit)
+ * pairs: the top-100 of the teacher per position in "Effektivnaya distillyatsiya
+ * znaniy" (malakhovai.ru, paragraph 2) and "Wissensdestillation mit deutlich
+ * weniger GPU-Speicher" (dailytechsnack.ch, section "Teacher-Ausgaben einmalig
+ * zwischenspeichern").  With temperature T ("Distillyatsiya i szhatie modeley",
+ * ml-book.com, section "Kak eto rabotaet: myagkie metki i temperatura"):
+ *
+ *   p_ik  = softmax_k(t_ik / T)                (renormalised over the K cached ids)
+ *   lse_i = logsumexp_v (z_iv / T)             (over the FULL vocabulary V)
+ *   KL_i  = sum_k p_ik (log p_ik - z_{i,idx_ik}/T + lse_i)      (0 log 0 = 0)
+ *   loss  = T^2 * sum_{valid i} KL_i / N_valid                  (0 if N_valid = 0)
+ *   dz_iv = g * valid_i * T * (exp(z_iv/T - lse_i) - s_iv) / N_valid,
+ *           s_iv = sum_{k: idx_ik = v} p_ik,   g = upstream gradient
+ *   dh = dz W,  dW = dz^T h
+ *
+ * A token is valid when mask_i != 0 and at least one of its teacher logits is
+ * finite.  The sequence is processed in chunks of rows: logits of a chunk are
+ * reduced and discarded, and recomputed in the backward pass ("Multiverse
+ * Computing uzhala distillyatsiyu", iitak.ru, paragraph 3; dailytechsnack.ch,
+ * section "KL-Verlust wird in Bloecken berechnet": the output projection feeds
+ * the loss directly).  Workspace grows linearly in N.
+ *
+ * Conventions shared by every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no device memory and keeps no state between calls.
+ *  - Layouts are dense row-major: h [N][d] bf16, W [V][d] bf16, idx [N][K]
+ *    int32, tlogit [N][K] fp32, mask [N] uint8 (NULL = every row valid),
+ *    lse [N] fp32, dh [N][d] bf16, dW [V][d] fp32.
+ *  - Preconditions checked on the host (FKL_ERR_INVALID_ARG, before any launch):
+ *    non-NULL required pointers; N >= 1; 8 <= d, d % 8 == 0; V >= 1, V % 8 == 0
+ *    is NOT required; 1 <= K <= 256, K <= V; T > 0 and finite; chunk == 0
+ *    (library default) or a positive multiple of 128; h, W, dh, dW and the
+ *    workspace 16-byte aligned.  Teacher ids within a row must be distinct
+ *    (not checked; repeated ids are summed into s).
+ *  - Calls enqueue on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *    and return without synchronising.  Errors found on the device (a teacher
+ *    id outside [0, V), a pipeline wait that timed out) are written to a status
+ *    word at the start of the workspace; read it with fkl_get_status.
+ *  - `ws` must hold at least fkl_workspace_size(N, d, V, K, chunk) bytes
+ *    (FKL_ERR_WORKSPACE otherwise).  The same workspace may serve the forward
+ *    and the backward call; its contents between calls carry no meaning except
+ *    the status word.
+ */
+#ifndef FKL_H
+#define FKL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FKL_OK = 0,
+    FKL_ERR_INVALID_ARG = 1,  /* a precondition above failed (host-side, nothing launched) */
+    FKL_ERR_WORKSPACE = 2,    /* ws_bytes below fkl_workspace_size */
+    FKL_ERR_INDEX = 3,        /* a teacher id outside [0, V); outputs are undefined */
+    FKL_ERR_CUDA = 4,         /* a CUDA runtime or driver call failed; see fkl_last_error */
+    FKL_ERR_UNSUPPORTED = 5,  /* no sm_103a device, or a size beyond the kernels' limits */
+    FKL_ERR_TIMEOUT = 6       /* a bounded pipeline wait gave up on the device */
+} fkl_status;
+
+/* Bytes of device workspace needed by fkl_forward and fkl_backward for these
+ * sizes (chunk as passed to them).  Pure host arithmetic; 0 if the sizes are
+ * invalid.  It is O(chunk * V + N): one bf16 dz chunk buffer, split-K partials
+ * of dh for one chunk, the sorted teacher cache of one chunk and 4 bytes per
+ * token. */
+size_t fkl_workspace_size(int64_t N, int d, int64_t V, int K, int chunk);
+
+/* Forward: writes loss (one fp32, device) and lse[N] (fp32, natural-log
+ * logsumexp of z/T for every row, masked rows included). */
+fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                       const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T,
+                       int chunk, float* loss, float* lse,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Backward: recomputes every logit tile and writes dh [N][d] (bf16, overwritten)
+ * and dW [V][d] (fp32, overwritten).  `lse` is the forward's output for the same
+ * inputs.  `grad_loss` points to one fp32 upstream gradient on the device
+ * (NULL = 1.0).  dW is accumulated chunk by chunk in a fixed order, so repeated
+ * calls give bit-identical results. */
+fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                        const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T,
+                        int chunk, const float* lse, const float* grad_loss,
+                        void* dh, float* dW,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream` and returns the device status word of `ws` (FKL_OK if
+ * no device-side error was recorded since the last call that used `ws`). */
+fkl_status fkl_get_status(const void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* fkl_status_string(fkl_status status);
+
+/* Message of the last host-side error in the calling thread ("" if none). */
+const char* fkl_last_error(void);
+
+/* ---- measurement hooks (not part of the loss) ----------------------------
+ * When enabled, every kernel launch of this library is bracketed by two CUDA
+ * events recorded on the launching stream.  fkl_profile_read synchronises the
+ * recorded events and reports, per kernel kind k < n, the summed device time in
+ * ms, the number of launches and the algorithmic FLOP those launches performed
+ * (tensor-core kernels only; 0 otherwise); it returns the number of kinds.
+ * fkl_profile_reset forgets the records.  Not thread-safe. */
+void fkl_profile_enable(int on);
+void fkl_profile_reset(void);
+int fkl_profile_read(double* ms, int64_t* launches, double* flop, int n);
+const char* fkl_kernel_name(int kind);
+/* Kernels launched by this library since it was loaded. */
+int64_t fkl_launch_count(void);
+
+/* ---- self-test entry (not part of the loss) -------------------------------
+ * C[M][N] (fp32, row-major) = sum_k A(m,k) B(n,k) on the same tcgen05/TMA
+ * pipeline the loss kernels use.  a_mn = 0: A is [M][K] row-major (K-major);
+ * a_mn = 1: A is stored [K][M] (M-major).  b_mn = 0: B is [N][K]; b_mn = 1: B
+ * is stored [K][N].  bn selects the N tile (256, 192 or 128).  M, N, K >= 1 and
+ * multiples of 8.  `ws` (>= 256 bytes, device) receives the status word.  Used
+ * to check the operand descriptors in isolation. */
+fkl_status fkl_selftest_gemm(const void* A, const void* B, float* C, int M, int N, int K,
+                             int a_mn, int b_mn, int bn, void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FKL_H */

@@ -1,0 +1,190 @@
+"""Torch-facing API over libfkl.so: forward, backward and an autograd loss.
+
+Every step of the loss runs in the library's CUDA kernels; this module only
+checks tensor properties, allocates outputs and the workspace with torch, and
+passes raw pointers plus the current CUDA stream.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+STATUS_NAMES = {0: "FKL_OK", 1: "FKL_ERR_INVALID_ARG", 2: "FKL_ERR_WORKSPACE", 3: "FKL_ERR_INDEX",
+                4: "FKL_ERR_CUDA", 5: "FKL_ERR_UNSUPPORTED", 6: "FKL_ERR_TIMEOUT"}
+
+
+class FKLError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        L = _lib.lib()
+        msg = L.fkl_last_error().decode()
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({L.fkl_status_string(status).decode()}){': ' + msg if msg else ''}")
+        self.status = status
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise FKLError(st, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _expect(t, name, dtype, ndim, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(N: int, d: int, V: int, K: int, chunk: int = 0) -> int:
+    n = _lib.lib().fkl_workspace_size(int(N), int(d), int(V), int(K), int(chunk))
+    if n == 0:
+        raise ValueError(f"invalid sizes N={N} d={d} V={V} K={K} chunk={chunk}")
+    return int(n)
+
+
+def alloc_workspace(N, d, V, K, chunk=0, device="cuda") -> torch.Tensor:
+    return torch.empty(workspace_size(N, d, V, K, chunk), dtype=torch.uint8, device=device)
+
+
+def _inputs(h, W, idx, tlogit, mask):
+    _expect(h, "h", torch.bfloat16, 2)
+    dev = h.device
+    _expect(W, "W", torch.bfloat16, 2, dev)
+    _expect(idx, "idx", torch.int32, 2, dev)
+    _expect(tlogit, "tlogit", torch.float32, 2, dev)
+    if mask is not None:
+        _expect(mask, "mask", torch.uint8, 1, dev)
+    N, d = h.shape
+    V, d2 = W.shape
+    if d2 != d:
+        raise ValueError(f"h is [N,{d}] but W is [V,{d2}]")
+    if idx.shape != tlogit.shape or idx.shape[0] != N:
+        raise ValueError("idx and tlogit must both be [N,K]")
+    if mask is not None and mask.shape[0] != N:
+        raise ValueError("mask must be [N]")
+    return N, d, V, idx.shape[1], dev
+
+
+def forward(h, W, idx, tlogit, mask=None, T: float = 1.0, chunk: int = 0,
+            ws: Optional[torch.Tensor] = None, loss: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Fused forward: returns (loss [1] fp32, lse [N] fp32) on h's device."""
+    N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
+    if ws is None:
+        ws = alloc_workspace(N, d, V, K, chunk, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
+    st = _lib.lib().fkl_forward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
+                                float(T), int(chunk), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
+                                _stream(dev))
+    _check(st, "fkl_forward")
+    return loss, lse
+
+
+def backward(h, W, idx, tlogit, mask, T: float, lse: torch.Tensor,
+             grad_loss: Optional[torch.Tensor] = None, chunk: int = 0,
+             ws: Optional[torch.Tensor] = None, dh: Optional[torch.Tensor] = None,
+             dW: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Fused backward: returns (dh [N,d] bf16, dW [V,d] fp32)."""
+    N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
+    _expect(lse, "lse", torch.float32, 1, dev)
+    if grad_loss is not None:
+        _expect(grad_loss.reshape(-1), "grad_loss", torch.float32, 1, dev)
+    if ws is None:
+        ws = alloc_workspace(N, d, V, K, chunk, dev)
+    dh = torch.empty((N, d), dtype=torch.bfloat16, device=dev) if dh is None else dh
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev) if dW is None else dW
+    st = _lib.lib().fkl_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
+                                 float(T), int(chunk), _ptr(lse), _ptr(grad_loss), _ptr(dh),
+                                 _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "fkl_backward")
+    return dh, dW
+
+
+def get_status(ws: torch.Tensor) -> int:
+    """Synchronises the current stream and returns the workspace's device status word."""
+    return int(_lib.lib().fkl_get_status(_ptr(ws), _stream(ws.device)))
+
+
+class FKLLoss(torch.autograd.Function):
+    """T^2 * mean over valid rows of KL(p_teacher || q_student); gradients for h and W."""
+
+    @staticmethod
+    def forward(ctx, h, W, idx, tlogit, mask, T, chunk):
+        N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
+        ws = alloc_workspace(N, d, V, K, chunk, dev)
+        loss, lse = forward(h, W, idx, tlogit, mask, T, chunk, ws=ws)
+        ctx.save_for_backward(h, W, idx, tlogit, lse)
+        ctx.mask, ctx.T, ctx.chunk, ctx.ws = mask, T, chunk, ws
+        return loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, g):
+        h, W, idx, tlogit, lse = ctx.saved_tensors
+        g = g.reshape(1).to(torch.float32).contiguous()
+        dh, dW = backward(h, W, idx, tlogit, ctx.mask, ctx.T, lse, grad_loss=g, chunk=ctx.chunk,
+                          ws=ctx.ws)
+        ctx.ws = None
+        return dh, dW.to(W.dtype), None, None, None, None, None
+
+
+def fkl_loss(h, W, idx, tlogit, mask=None, T: float = 1.0, chunk: int = 0) -> torch.Tensor:
+    """Autograd-aware fused loss (scalar)."""
+    return FKLLoss.apply(h, W, idx, tlogit, mask, T, chunk)
+
+
+# ---- measurement hooks -------------------------------------------------------
+def profile_enable(on: bool = True):
+    _lib.lib().fkl_profile_enable(1 if on else 0)
+
+
+def profile_reset():
+    _lib.lib().fkl_profile_reset()
+
+
+def profile_read() -> dict:
+    """{kernel name: (total ms, launches, algorithmic FLOP)} of the recorded launches."""
+    L = _lib.lib()
+    n = 16
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    fl = (ctypes.c_double * n)()
+    k = L.fkl_profile_read(ms, cnt, fl, n)
+    return {L.fkl_kernel_name(i).decode(): (ms[i], int(cnt[i]), fl[i]) for i in range(k) if cnt[i]}
+
+
+def launch_count() -> int:
+    return int(_lib.lib().fkl_launch_count())
+
+
+def selftest_gemm(A: torch.Tensor, B: torch.Tensor, M: int, N: int, K: int, a_mn: int, b_mn: int,
+                  bn: int = 256) -> torch.Tensor:
+    """C = A . B^T on the library's tcgen05 pipeline (see fkl_selftest_gemm)."""
+    C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    ws = torch.zeros(256, dtype=torch.uint8, device=A.device)
+    st = _lib.lib().fkl_selftest_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, a_mn, b_mn, bn, _ptr(ws),
+                                      _stream(A.device))
+    _check(st, "fkl_selftest_gemm")
+    s = get_status(ws)
+    if s != 0:
+        raise FKLError(s, "fkl_selftest_gemm (device)")
+    return C

@@ -1,0 +1,223 @@
+// CUDA-core kernels around the tensor-core GEMMs: teacher preparation, the
+// per-row merge of the forward partials, the deterministic loss reduction, the
+// split-K reduction of dh and the count of valid rows.
+#include <climits>
+#include <cmath>
+
+#include <cuda_bf16.h>
+
+#include "fkl_internal.h"
+
+namespace fkl {
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// N_valid = #{i : mask_i != 0 and some teacher logit of row i is finite}.  One warp per row.
+__global__ void count_valid_kernel(const float* __restrict__ t, const uint8_t* __restrict__ mask,
+                                   int64_t N, int K, int* __restrict__ n_valid) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    int count = 0;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < N;
+         r += warps) {
+        if (mask && mask[r] == 0) continue;  // warp-uniform
+        bool fin = false;
+        for (int k = lane; k < K; k += 32) fin |= isfinite(t[r * K + k]);
+        if (__any_sync(0xffffffffu, fin)) ++count;
+    }
+    __shared__ int s_cnt;
+    if (threadIdx.x == 0) s_cnt = 0;
+    __syncthreads();
+    if (lane == 0 && count) atomicAdd(&s_cnt, count);
+    __syncthreads();
+    if (threadIdx.x == 0 && s_cnt) atomicAdd(n_valid, s_cnt);
+}
+
+// Per row of a chunk (one warp per row): p = softmax(t/T) over the K cached
+// entries, H = sum p log p, validity, and (id, p) sorted by id.  Ids outside
+// [0, V) raise FKL_ERR_INDEX and are replaced by INT_MAX, which no tile reaches.
+__global__ void teacher_prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ t,
+                                    const uint8_t* __restrict__ mask, int64_t row0, int rows, int K,
+                                    int64_t V, float T, int* __restrict__ sidx, float* __restrict__ sp,
+                                    float* __restrict__ H, uint8_t* __restrict__ valid,
+                                    int* __restrict__ status) {
+    __shared__ int s_ix[4][kMaxK];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 4 + w;
+    if (r >= rows) return;
+    const int64_t gr = row0 + r;
+    const int32_t* ir = idx + gr * K;
+    const float* tr = t + gr * K;
+    constexpr int PER = kMaxK / 32;
+    int ix[PER];
+    float u[PER];
+    float mx = -INFINITY;
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int k = lane + 32 * j;
+        ix[j] = INT_MAX;
+        u[j] = -INFINITY;
+        if (k < K) {
+            int id = ir[k];
+            if (id < 0 || static_cast<int64_t>(id) >= V) {
+                bad = true;
+                id = INT_MAX;
+            }
+            ix[j] = id;
+            const float tv = tr[k];
+            u[j] = isfinite(tv) ? tv / T : -INFINITY;  // non-finite logits carry no mass
+            mx = fmaxf(mx, u[j]);
+        }
+    }
+    if (bad) atomicCAS(status, 0, static_cast<int>(FKL_ERR_INDEX));
+    mx = warp_max(mx);
+    const bool has_mass = mx > -INFINITY;
+    float e[PER];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        e[j] = (has_mass && u[j] > -INFINITY) ? expf(u[j] - mx) : 0.f;
+        s += e[j];
+    }
+    s = warp_sum(s);
+    float hs = 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        e[j] = has_mass ? e[j] / s : 0.f;
+        if (e[j] > 0.f) hs += e[j] * logf(e[j]);
+    }
+    hs = warp_sum(hs);
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int k = lane + 32 * j;
+        if (k < K) s_ix[w][k] = ix[j];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int k = lane + 32 * j;
+        if (k < K) {
+            const int me = ix[j];
+            int rank = 0;
+            for (int i = 0; i < K; ++i) {
+                const int o = s_ix[w][i];
+                rank += (o < me) || (o == me && i < k);
+            }
+            sidx[static_cast<size_t>(r) * K + rank] = me;
+            sp[static_cast<size_t>(r) * K + rank] = e[j];
+        }
+    }
+    if (lane == 0) {
+        H[r] = hs;
+        valid[r] = static_cast<uint8_t>((mask == nullptr || mask[gr] != 0) && has_mass);
+    }
+}
+
+// lse_i and KL_i of one chunk from the per-tile partials (fixed tile order).
+__global__ void fwd_finalize_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
+                                    const float* __restrict__ pg, int stride, int ntiles, int rows,
+                                    const float* __restrict__ H, const uint8_t* __restrict__ valid,
+                                    float T, float* __restrict__ lse, float* __restrict__ rowloss) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows) return;
+    float M = -INFINITY, L = 0.f, G = 0.f;
+    for (int n = 0; n < ntiles; ++n) {
+        const size_t o = static_cast<size_t>(n) * stride + r;
+        const float m = pm[o], l = pl[o];
+        G += pg[o];
+        if (m > M) {
+            L = L * exp2f(M - m) + l;
+            M = m;
+        } else {
+            L += l * exp2f(m - M);
+        }
+    }
+    const float lse_r = (M + log2f(L)) * 0.69314718055994531f;
+    lse[r] = lse_r;
+    rowloss[r] = valid[r] ? (H[r] - G / T + lse_r) : 0.f;
+}
+
+// loss = T^2 * sum_i rowloss_i / N_valid, summed in fp64 in a fixed order by one block.
+__global__ void loss_reduce_kernel(const float* __restrict__ rowloss, int64_t N,
+                                   const int* __restrict__ n_valid, float T, float* __restrict__ loss) {
+    __shared__ double s_part[1024];
+    double acc = 0.0;
+    for (int64_t i = threadIdx.x; i < N; i += blockDim.x) acc += static_cast<double>(rowloss[i]);
+    s_part[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = blockDim.x >> 1; w > 0; w >>= 1) {
+        if (static_cast<int>(threadIdx.x) < w) s_part[threadIdx.x] += s_part[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const int nv = *n_valid;
+        loss[0] = nv > 0 ? static_cast<float>(static_cast<double>(T) * T * s_part[0] / nv) : 0.f;
+    }
+}
+
+// dh[r][j] = bf16(sum_s part[s][r][j]) for the rows of one chunk.
+__global__ void dh_reduce_kernel(const float4* __restrict__ part, int splits, size_t split_elems4,
+                                 size_t n4, uint2* __restrict__ dh) {
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        float4 a = part[i];
+        for (int s = 1; s < splits; ++s) {
+            const float4 b = part[s * split_elems4 + i];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&lo);
+        o.y = *reinterpret_cast<uint32_t*>(&hi);
+        dh[i] = o;
+    }
+}
+
+void launch_count_valid(const float* tlogit, const uint8_t* mask, int64_t N, int K, int* n_valid,
+                        int grid, cudaStream_t s) {
+    count_valid_kernel<<<grid, 256, 0, s>>>(tlogit, mask, N, K, n_valid);
+}
+
+void launch_teacher_prep(const int32_t* idx, const float* tlogit, const uint8_t* mask, int64_t row0,
+                         int rows, int K, int64_t V, float T, int* sidx, float* sp, float* H,
+                         uint8_t* valid, int* status, cudaStream_t s) {
+    teacher_prep_kernel<<<(rows + 3) / 4, 128, 0, s>>>(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H,
+                                                       valid, status);
+}
+
+void launch_fwd_finalize(const float* pm, const float* pl, const float* pg, int stride, int ntiles,
+                         int rows, const float* H, const uint8_t* valid, float T, float* lse,
+                         float* rowloss, cudaStream_t s) {
+    fwd_finalize_kernel<<<(rows + 127) / 128, 128, 0, s>>>(pm, pl, pg, stride, ntiles, rows, H, valid, T,
+                                                           lse, rowloss);
+}
+
+void launch_loss_reduce(const float* rowloss, int64_t N, const int* n_valid, float T, float* loss,
+                        cudaStream_t s) {
+    loss_reduce_kernel<<<1, 1024, 0, s>>>(rowloss, N, n_valid, T, loss);
+}
+
+void launch_dh_reduce(const float* part, int splits, size_t split_elems, int rows, int d, void* dh,
+                      cudaStream_t s) {
+    const size_t n4 = static_cast<size_t>(rows) * d / 4;
+    int grid = static_cast<int>((n4 + 255) / 256);
+    if (grid > 148 * 8) grid = 148 * 8;
+    if (grid < 1) grid = 1;
+    dh_reduce_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(part), splits, split_elems / 4,
+                                         n4, reinterpret_cast<uint2*>(dh));
+}
+
+}  // namespace fkl

@@ -1,0 +1,571 @@
+// Host side of libfkl.so: argument checks, the sequence-chunk plan, TMA
+// descriptors and the launch sequence of the forward and backward passes.
+//
+// Forward, per chunk of C rows ("Multiverse Computing uzhala distillyatsiyu",
+// iitak.ru, paragraph 3: a chunk's student probabilities are reduced into the
+// running total and dropped):
+//   teacher_prep -> fwd GEMM with the logsumexp / gather epilogue -> finalize
+// then one deterministic loss reduction over all rows.
+// Backward, per chunk (logits recomputed rather than stored, same paragraph and
+// "Wissensdestillation mit deutlich weniger GPU-Speicher", dailytechsnack.ch,
+// section "KL-Verlust wird in Bloecken berechnet"):
+//   teacher_prep -> dz GEMM (recompute + dz in bf16) -> dh GEMM (split over V)
+//   -> dh reduction -> dW GEMM (store for the first chunk, reduce-add after).
+// All launches go to the caller's stream; nothing synchronises.
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "fkl_internal.h"
+
+namespace fkl {
+namespace {
+
+thread_local char g_err[512] = "";
+
+fkl_status fail(fkl_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+fkl_status fail(fkl_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+std::atomic<int64_t> g_launches{0};
+
+// ---------------------------------------------------------------- profiling hooks
+struct ProfRec {
+    int kind;
+    double flop;
+    cudaEvent_t a, b;
+};
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pool_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+struct LaunchScope {
+    ProfRec rec{};
+    cudaStream_t s;
+    LaunchScope(int kind, double flop, cudaStream_t st) : s(st) {
+        rec.kind = kind;
+        rec.flop = flop;
+        if (g_prof_on) {
+            rec.a = pool_event();
+            rec.b = pool_event();
+            cudaEventRecord(rec.a, s);
+        }
+    }
+    ~LaunchScope() {
+        ++g_launches;
+        if (g_prof_on) {
+            cudaEventRecord(rec.b, s);
+            g_prof.push_back(rec);
+        }
+    }
+};
+
+const char* const kKindNames[KK_NUM] = {
+    "count_valid", "teacher_prep", "fwd_gemm_lse", "fwd_finalize", "loss_reduce",
+    "bwd_gemm_dz", "bwd_gemm_dh", "dh_reduce", "bwd_gemm_dw", "selftest_gemm",
+};
+
+// ---------------------------------------------------------------- device facts
+struct DeviceInfo {
+    bool ok = false;
+    int sms = 0;
+    char why[160] = "";
+};
+
+DeviceInfo query_device() {
+    DeviceInfo di;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        snprintf(di.why, sizeof(di.why), "no CUDA device");
+        cudaGetLastError();
+        return di;
+    }
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) {
+        snprintf(di.why, sizeof(di.why), "device %d is sm_%d%d; libfkl is built for sm_103a only", dev,
+                 major, minor);
+        return di;
+    }
+    di.ok = true;
+    return di;
+}
+
+const DeviceInfo& device_info() {
+    static std::once_flag once;
+    static DeviceInfo di;
+    std::call_once(once, [] { di = query_device(); });
+    return di;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D tiled tensor map with 128-byte swizzle: dim0 is contiguous.
+bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+               uint64_t stride1_bytes, uint32_t box0, uint32_t box1) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {dim0, dim1};
+    cuuint64_t strides[1] = {stride1_bytes};
+    cuuint32_t box[2] = {box0, box1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- the plan
+constexpr int kDefaultChunk = 4096;
+constexpr int kMaxChunk = 1 << 20;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Plan {
+    int64_t N, V, Vs, n_chunks;
+    int d, K, Cc, nt_v, bn_d, nt_d, splits;
+    size_t o_sidx, o_sp, o_H, o_valid, o_rowloss, o_big, o_part_dh, total;
+};
+
+int pick_bn(int d) {
+    const int cands[3] = {256, 192, 128};
+    int best = 256;
+    int64_t best_waste = INT64_MAX;
+    for (int c : cands) {
+        const int64_t waste = cdiv(d, c) * c - d;
+        if (waste < best_waste) {
+            best_waste = waste;
+            best = c;
+        }
+    }
+    return best;
+}
+
+int pick_splits(int m_tiles, int n_tiles, int64_t kb_total) {
+    auto eff = [&](int s) {
+        const int64_t units = int64_t(m_tiles) * n_tiles * s;
+        const int64_t waves = cdiv(units, kPlanSMs);
+        return double(units) / double(waves * kPlanSMs);
+    };
+    int best = 1;
+    for (int s = 2; s <= 8; ++s) {
+        if (s > kb_total / 2) break;
+        if (eff(s) > eff(best) + 0.02) best = s;
+    }
+    return best;
+}
+
+const char* check_sizes(int64_t N, int d, int64_t V, int K, int chunk) {
+    if (N < 1) return "N must be >= 1";
+    if (d < 8 || d % 8 != 0) return "d must be a positive multiple of 8";
+    if (d > 65536) return "d above 65536 is not supported";
+    if (V < 1 || V > (int64_t(1) << 30)) return "V must be in [1, 2^30]";
+    if (K < 1 || K > kMaxK) return "K must be in [1, 256]";
+    if (K > V) return "K must not exceed V";
+    if (chunk < 0 || chunk % kBM != 0 || chunk > kMaxChunk)
+        return "chunk must be 0 (default) or a positive multiple of 128 up to 2^20";
+    if (N > (int64_t(1) << 40)) return "N too large";
+    return nullptr;
+}
+
+bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
+    if (check_sizes(N, d, V, K, chunk)) return false;
+    P.N = N;
+    P.d = d;
+    P.V = V;
+    P.K = K;
+    const int64_t want = chunk > 0 ? chunk : kDefaultChunk;
+    P.Cc = static_cast<int>(std::min<int64_t>(want, cdiv(N, kBM) * kBM));
+    P.n_chunks = cdiv(N, P.Cc);
+    P.nt_v = static_cast<int>(cdiv(V, kVocabTile));
+    P.bn_d = pick_bn(d);
+    P.nt_d = static_cast<int>(cdiv(d, P.bn_d));
+    P.splits = pick_splits(static_cast<int>(cdiv(P.Cc, kBM)), P.nt_d, cdiv(V, kBK));
+    P.Vs = cdiv(V, 8) * 8;
+    size_t off = 256;  // header: status word, N_valid
+    P.o_sidx = off;
+    off += align256(size_t(P.Cc) * K * 4);
+    P.o_sp = off;
+    off += align256(size_t(P.Cc) * K * 4);
+    P.o_H = off;
+    off += align256(size_t(P.Cc) * 4);
+    P.o_valid = off;
+    off += align256(size_t(P.Cc));
+    P.o_rowloss = off;
+    off += align256(size_t(N) * 4);
+    P.o_big = off;
+    const size_t part_fwd = 3 * align256(size_t(P.nt_v) * P.Cc * 4);
+    const size_t dz = align256(size_t(P.Cc) * P.Vs * 2);
+    const size_t part_dh = size_t(P.splits) * P.Cc * d * 4;
+    P.o_part_dh = P.o_big + dz;
+    P.total = P.o_big + std::max(part_fwd, dz + part_dh);
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+const char* check_common(const void* h, const void* W, const int32_t* idx, const float* tlogit, int64_t N,
+                         int d, int64_t V, int K, float T, int chunk, const void* ws) {
+    if (!h || !W || !idx || !tlogit || !ws) return "null input or workspace pointer";
+    if (const char* e = check_sizes(N, d, V, K, chunk)) return e;
+    if (!(T > 0.f) || !std::isfinite(T)) return "T must be positive and finite";
+    if (!aligned16(h) || !aligned16(W) || !aligned16(ws)) return "h, W and ws must be 16-byte aligned";
+    return nullptr;
+}
+
+#define FKL_CUDA_TRY(expr)                                                                        \
+    do {                                                                                          \
+        cudaError_t e_ = (expr);                                                                  \
+        if (e_ != cudaSuccess) return fail(FKL_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+    } while (0)
+
+fkl_status device_ready() {
+    const DeviceInfo& di = device_info();
+    if (!di.ok) return fail(FKL_ERR_UNSUPPORTED, "%s", di.why);
+    if (!encode_fn()) return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    return FKL_OK;
+}
+
+fkl_status run_gemm(int kind, int bn, int a_mn, int b_mn, int epi, const CUtensorMap& a, const CUtensorMap& b,
+                    const CUtensorMap& o, const GemmParams& p, double flop, cudaStream_t s) {
+    const int64_t units = int64_t(p.m_tiles) * p.n_tiles * p.splits;
+    const int grid = static_cast<int>(std::min<int64_t>(units, device_info().sms));
+    cudaError_t e;
+    {
+        LaunchScope ls(kind, flop, s);
+        e = launch_gemm(bn, a_mn, b_mn, epi, a, b, o, p, grid, s);
+    }
+    if (e != cudaSuccess) return fail(FKL_ERR_CUDA, "%s launch: %s", kKindNames[kind], cudaGetErrorString(e));
+    return FKL_OK;
+}
+
+#define FKL_TMAP(m, ...)                                                          \
+    do {                                                                          \
+        if (!make_tmap(&(m), __VA_ARGS__))                                        \
+            return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for " #m);   \
+    } while (0)
+
+#define FKL_SMALL(kind, call)                                                                     \
+    do {                                                                                          \
+        {                                                                                         \
+            LaunchScope ls_((kind), 0.0, s);                                                      \
+            call;                                                                                 \
+        }                                                                                         \
+        cudaError_t e_ = cudaGetLastError();                                                      \
+        if (e_ != cudaSuccess)                                                                    \
+            return fail(FKL_ERR_CUDA, "%s launch: %s", kKindNames[kind], cudaGetErrorString(e_)); \
+    } while (0)
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+constexpr auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+
+}  // namespace
+}  // namespace fkl
+
+using namespace fkl;
+
+extern "C" {
+
+size_t fkl_workspace_size(int64_t N, int d, int64_t V, int K, int chunk) {
+    Plan P;
+    return make_plan(N, d, V, K, chunk, P) ? P.total : 0;
+}
+
+const char* fkl_status_string(fkl_status st) {
+    switch (st) {
+        case FKL_OK: return "ok";
+        case FKL_ERR_INVALID_ARG: return "invalid argument";
+        case FKL_ERR_WORKSPACE: return "workspace too small";
+        case FKL_ERR_INDEX: return "teacher index outside [0, V)";
+        case FKL_ERR_CUDA: return "CUDA error";
+        case FKL_ERR_UNSUPPORTED: return "unsupported device or size";
+        case FKL_ERR_TIMEOUT: return "device pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* fkl_last_error(void) { return g_err; }
+
+fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                       const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T, int chunk,
+                       float* loss, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    g_err[0] = 0;
+    if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
+        return fail(FKL_ERR_INVALID_ARG, "%s", e);
+    if (!loss || !lse) return fail(FKL_ERR_INVALID_ARG, "null loss or lse pointer");
+    Plan P;
+    make_plan(N, d, V, K, chunk, P);
+    if (ws_bytes < P.total)
+        return fail(FKL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, P.total);
+    if (fkl_status st = device_ready()) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(ws);
+    int* status = reinterpret_cast<int*>(w);
+    int* n_valid = status + 1;
+    int* sidx = reinterpret_cast<int*>(w + P.o_sidx);
+    float* sp = reinterpret_cast<float*>(w + P.o_sp);
+    float* H = reinterpret_cast<float*>(w + P.o_H);
+    uint8_t* valid = reinterpret_cast<uint8_t*>(w + P.o_valid);
+    float* rowloss = reinterpret_cast<float*>(w + P.o_rowloss);
+    const size_t pstride = align256(size_t(P.nt_v) * P.Cc * 4);
+    float* pm = reinterpret_cast<float*>(w + P.o_big);
+    float* pl = reinterpret_cast<float*>(w + P.o_big + pstride);
+    float* pg = reinterpret_cast<float*>(w + P.o_big + 2 * pstride);
+
+    FKL_CUDA_TRY(cudaMemsetAsync(w, 0, 256, s));
+    const int sms = device_info().sms;
+    FKL_SMALL(KK_COUNT_VALID, launch_count_valid(tlogit, mask, N, K, n_valid, sms * 4, s));
+
+    CUtensorMap tmW;
+    FKL_TMAP(tmW, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 256);
+    for (int64_t c = 0; c < P.n_chunks; ++c) {
+        const int64_t row0 = c * P.Cc;
+        const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
+        FKL_SMALL(KK_TEACHER_PREP,
+                  launch_teacher_prep(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status, s));
+        CUtensorMap tmH;
+        FKL_TMAP(tmH, BF16, static_cast<const char*>(h) + size_t(row0) * d * 2, uint64_t(d), uint64_t(rows),
+                 uint64_t(d) * 2, 64, 128);
+        GemmParams p{};
+        p.m_tiles = static_cast<int>(cdiv(rows, kBM));
+        p.n_tiles = P.nt_v;
+        p.splits = 1;
+        p.kb_total = static_cast<int>(cdiv(d, kBK));
+        p.m_fastest = 1;
+        p.M = rows;
+        p.Ncols = static_cast<int>(V);
+        p.status = status;
+        p.scale2 = kLog2e / T;
+        p.sidx = sidx;
+        p.sp = sp;
+        p.K = K;
+        p.part_m = pm;
+        p.part_l = pl;
+        p.part_g = pg;
+        p.part_stride = P.Cc;
+        if (fkl_status st = run_gemm(KK_FWD_LSE, 256, 0, 0, EPI_LSE, tmH, tmW, tmW, p,
+                                     2.0 * rows * double(d) * double(V), s))
+            return st;
+        FKL_SMALL(KK_FWD_FINALIZE,
+                  launch_fwd_finalize(pm, pl, pg, P.Cc, P.nt_v, rows, H, valid, T, lse + row0, rowloss + row0, s));
+    }
+    FKL_SMALL(KK_LOSS_REDUCE, launch_loss_reduce(rowloss, N, n_valid, T, loss, s));
+    return FKL_OK;
+}
+
+fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                        const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T, int chunk,
+                        const float* lse, const float* grad_loss, void* dh, float* dW, void* ws,
+                        size_t ws_bytes, void* stream) {
+    g_err[0] = 0;
+    if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
+        return fail(FKL_ERR_INVALID_ARG, "%s", e);
+    if (!lse || !dh || !dW) return fail(FKL_ERR_INVALID_ARG, "null lse, dh or dW pointer");
+    if (!aligned16(dh) || !aligned16(dW)) return fail(FKL_ERR_INVALID_ARG, "dh and dW must be 16-byte aligned");
+    Plan P;
+    make_plan(N, d, V, K, chunk, P);
+    if (ws_bytes < P.total)
+        return fail(FKL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, P.total);
+    if (fkl_status st = device_ready()) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(ws);
+    int* status = reinterpret_cast<int*>(w);
+    int* n_valid = status + 1;
+    int* sidx = reinterpret_cast<int*>(w + P.o_sidx);
+    float* sp = reinterpret_cast<float*>(w + P.o_sp);
+    float* H = reinterpret_cast<float*>(w + P.o_H);
+    uint8_t* valid = reinterpret_cast<uint8_t*>(w + P.o_valid);
+    void* dz = w + P.o_big;
+    float* part = reinterpret_cast<float*>(w + P.o_part_dh);
+
+    FKL_CUDA_TRY(cudaMemsetAsync(w, 0, 256, s));
+    const int sms = device_info().sms;
+    FKL_SMALL(KK_COUNT_VALID, launch_count_valid(tlogit, mask, N, K, n_valid, sms * 4, s));
+
+    CUtensorMap tmW_k, tmW_mn, tmDW;
+    FKL_TMAP(tmW_k, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 256);
+    FKL_TMAP(tmW_mn, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 64);
+    FKL_TMAP(tmDW, F32, dW, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32);
+    for (int64_t c = 0; c < P.n_chunks; ++c) {
+        const int64_t row0 = c * P.Cc;
+        const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
+        const double flop = 2.0 * rows * double(d) * double(V);
+        FKL_SMALL(KK_TEACHER_PREP,
+                  launch_teacher_prep(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status, s));
+        const char* hc = static_cast<const char*>(h) + size_t(row0) * d * 2;
+        CUtensorMap tmH_k, tmH_mn, tmDz_st, tmDz_k, tmDz_mn, tmPart;
+        FKL_TMAP(tmH_k, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 128);
+        FKL_TMAP(tmH_mn, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 64);
+        FKL_TMAP(tmDz_st, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 32);
+        FKL_TMAP(tmDz_k, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 128);
+        FKL_TMAP(tmDz_mn, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 64);
+        FKL_TMAP(tmPart, F32, part, uint64_t(d), uint64_t(P.splits) * P.Cc, uint64_t(d) * 4, 32, 32);
+
+        // dz = T g (q - s) / N_valid for this chunk's rows, bf16 [rows][V]
+        GemmParams p{};
+        p.m_tiles = static_cast<int>(cdiv(rows, kBM));
+        p.n_tiles = P.nt_v;
+        p.splits = 1;
+        p.kb_total = static_cast<int>(cdiv(d, kBK));
+        p.m_fastest = 1;
+        p.M = rows;
+        p.Ncols = static_cast<int>(V);
+        p.status = status;
+        p.scale2 = kLog2e / T;
+        p.sidx = sidx;
+        p.sp = sp;
+        p.K = K;
+        p.lse = lse + row0;
+        p.valid = valid;
+        p.n_valid = n_valid;
+        p.grad = grad_loss;
+        p.T = T;
+        if (fkl_status st = run_gemm(KK_BWD_DZ, 256, 0, 0, EPI_DZ, tmH_k, tmW_k, tmDz_st, p, flop, s)) return st;
+
+        // dh partials: [split][rows][d] = dz[:, split's V range] W[split's V range, :]
+        GemmParams q{};
+        q.m_tiles = static_cast<int>(cdiv(rows, kBM));
+        q.n_tiles = P.nt_d;
+        q.splits = P.splits;
+        q.kb_total = static_cast<int>(cdiv(V, kBK));
+        q.m_fastest = 1;
+        q.M = rows;
+        q.Ncols = d;
+        q.status = status;
+        q.split_row_stride = P.Cc;
+        q.reduce = 0;
+        if (fkl_status st = run_gemm(KK_BWD_DH, P.bn_d, 0, 1, EPI_F32, tmDz_k, tmW_mn, tmPart, q, flop, s))
+            return st;
+        FKL_SMALL(KK_DH_REDUCE, launch_dh_reduce(part, P.splits, size_t(P.Cc) * d, rows, d,
+                                                 static_cast<char*>(dh) + size_t(row0) * d * 2, s));
+
+        // dW (+)= dz^T h_chunk, one owner per output tile, chunks in order
+        GemmParams r{};
+        r.m_tiles = static_cast<int>(cdiv(V, kBM));
+        r.n_tiles = P.nt_d;
+        r.splits = 1;
+        r.kb_total = static_cast<int>(cdiv(rows, kBK));
+        r.m_fastest = 0;
+        r.M = static_cast<int>(V);
+        r.Ncols = d;
+        r.status = status;
+        r.reduce = c > 0 ? 1 : 0;
+        if (fkl_status st = run_gemm(KK_BWD_DW, P.bn_d, 1, 1, EPI_F32, tmDz_mn, tmH_mn, tmDW, r, flop, s))
+            return st;
+    }
+    return FKL_OK;
+}
+
+fkl_status fkl_get_status(const void* ws, void* stream) {
+    g_err[0] = 0;
+    if (!ws) return fail(FKL_ERR_INVALID_ARG, "null workspace");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FKL_CUDA_TRY(cudaStreamSynchronize(s));
+    int st = 0;
+    FKL_CUDA_TRY(cudaMemcpy(&st, ws, sizeof(int), cudaMemcpyDeviceToHost));
+    return static_cast<fkl_status>(st);
+}
+
+void fkl_profile_enable(int on) { g_prof_on = on != 0; }
+
+void fkl_profile_reset(void) {
+    for (auto& r : g_prof) {
+        g_event_pool.push_back(r.a);
+        g_event_pool.push_back(r.b);
+    }
+    g_prof.clear();
+}
+
+int fkl_profile_read(double* ms, int64_t* launches, double* flop, int n) {
+    for (int k = 0; k < n && k < KK_NUM; ++k) {
+        if (ms) ms[k] = 0;
+        if (launches) launches[k] = 0;
+        if (flop) flop[k] = 0;
+    }
+    for (auto& r : g_prof) {
+        if (r.kind >= n) continue;
+        float t = 0.f;
+        cudaEventSynchronize(r.b);
+        cudaEventElapsedTime(&t, r.a, r.b);
+        if (ms) ms[r.kind] += t;
+        if (launches) launches[r.kind] += 1;
+        if (flop) flop[r.kind] += r.flop;
+    }
+    return KK_NUM;
+}
+
+const char* fkl_kernel_name(int kind) { return (kind >= 0 && kind < KK_NUM) ? kKindNames[kind] : ""; }
+
+int64_t fkl_launch_count(void) { return g_launches.load(); }
+
+fkl_status fkl_selftest_gemm(const void* A, const void* B, float* C, int M, int N, int K, int a_mn, int b_mn,
+                             int bn, void* ws, void* stream) {
+    g_err[0] = 0;
+    if (!A || !B || !C || !ws) return fail(FKL_ERR_INVALID_ARG, "null pointer");
+    if (M < 1 || N < 1 || K < 1 || M % 8 || N % 8 || K % 8)
+        return fail(FKL_ERR_INVALID_ARG, "M, N, K must be positive multiples of 8");
+    if ((a_mn | b_mn) & ~1) return fail(FKL_ERR_INVALID_ARG, "a_mn and b_mn must be 0 or 1");
+    if (bn != 256 && bn != 192 && bn != 128) return fail(FKL_ERR_INVALID_ARG, "bn must be 256, 192 or 128");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(ws))
+        return fail(FKL_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (fkl_status st = device_ready()) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FKL_CUDA_TRY(cudaMemsetAsync(ws, 0, 256, s));
+    CUtensorMap ta, tb, tc;
+    if (a_mn == 0) FKL_TMAP(ta, BF16, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, 64, 128);
+    else FKL_TMAP(ta, BF16, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, 64);
+    if (b_mn == 0) FKL_TMAP(tb, BF16, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, 64, uint32_t(bn));
+    else FKL_TMAP(tb, BF16, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, 64);
+    FKL_TMAP(tc, F32, C, uint64_t(N), uint64_t(M), uint64_t(N) * 4, 32, 32);
+    GemmParams p{};
+    p.m_tiles = static_cast<int>(cdiv(M, kBM));
+    p.n_tiles = static_cast<int>(cdiv(N, bn));
+    p.splits = 1;
+    p.kb_total = static_cast<int>(cdiv(K, kBK));
+    p.m_fastest = 1;
+    p.M = M;
+    p.Ncols = N;
+    p.status = static_cast<int*>(ws);
+    return run_gemm(KK_SELFTEST, bn, a_mn, b_mn, EPI_F32, ta, tb, tc, p, 2.0 * M * double(N) * K, s);
+}
+
+}  // extern "C"

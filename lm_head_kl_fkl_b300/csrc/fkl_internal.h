@@ -1,0 +1,86 @@
+// Internal declarations shared by the host scheduler and the kernels of libfkl.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fkl.h"
+
+namespace fkl {
+
+constexpr int kBM = 128;          // rows of one UMMA tile (TMEM lanes)
+constexpr int kBK = 64;           // K elements per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int kVocabTile = 256;   // vocabulary columns per tile in the logit GEMMs
+constexpr int kThreads = 192;     // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
+constexpr int kPlanSMs = 148;     // SM count the workspace plan is sized for (B300)
+constexpr int kMaxK = 256;        // teacher entries per token
+
+// Kernel kinds, for the launch counter and the profiling hooks.
+enum KernelKind {
+    KK_COUNT_VALID = 0,
+    KK_TEACHER_PREP,
+    KK_FWD_LSE,      // tcgen05 GEMM z = h W^T + online logsumexp / teacher gather epilogue
+    KK_FWD_FINALIZE,
+    KK_LOSS_REDUCE,
+    KK_BWD_DZ,       // tcgen05 GEMM recompute of z + dz epilogue (bf16, TMA store)
+    KK_BWD_DH,       // tcgen05 GEMM dh partials = dz W (split over V)
+    KK_DH_REDUCE,
+    KK_BWD_DW,       // tcgen05 GEMM dW (+)= dz^T h (TMA store / reduce-add)
+    KK_SELFTEST,
+    KK_NUM
+};
+
+enum Epilogue { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2 };
+
+// Parameters of one persistent GEMM launch.  The unit space is
+// m_tiles x n_tiles x splits; unit u maps to (m, n, s) with s slowest and either
+// m (m_fastest = 1) or n fastest; split s covers k-blocks
+// [s * kb_total / splits, (s + 1) * kb_total / splits).
+struct GemmParams {
+    int m_tiles, n_tiles, splits, kb_total, m_fastest;
+    int M;             // valid rows of the output (rows beyond are not written)
+    int Ncols;         // valid columns (V for the logit GEMMs, d for dh / dW)
+    int* status;       // device status word
+    // EPI_LSE / EPI_DZ
+    float scale2;      // log2(e) / T
+    const int* sidx;   // [M][K] teacher ids sorted ascending (chunk-local rows)
+    const float* sp;   // [M][K] teacher probabilities in the same order
+    int K;
+    float* part_m;     // EPI_LSE: [n_tiles][part_stride] running max (base 2)
+    float* part_l;     //          [n_tiles][part_stride] sum of 2^(y - max)
+    float* part_g;     //          [n_tiles][part_stride] sum_k p_k z_{idx_k}
+    int part_stride;
+    const float* lse;      // EPI_DZ: [M] natural-log lse of z/T
+    const uint8_t* valid;  // EPI_DZ: [M]
+    const int* n_valid;    // EPI_DZ: device scalar
+    const float* grad;     // EPI_DZ: device scalar or nullptr (1.0)
+    float T;
+    // EPI_F32
+    int split_row_stride;  // output row offset per split (dh partials), 0 otherwise
+    int reduce;            // 1: TMA reduce-add into the output, 0: TMA store
+};
+
+// Launch helpers implemented in gemm_tc.cu.  Return cudaSuccess or the launch error.
+cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& tmA,
+                        const CUtensorMap& tmB, const CUtensorMap& tmOut, const GemmParams& p,
+                        int grid, cudaStream_t stream);
+size_t gemm_smem_bytes(int bn, int epi);
+int gemm_stages(int bn);
+
+// Small kernels implemented in aux_kernels.cu.
+void launch_count_valid(const float* tlogit, const uint8_t* mask, int64_t N, int K, int* n_valid,
+                        int grid, cudaStream_t s);
+void launch_teacher_prep(const int32_t* idx, const float* tlogit, const uint8_t* mask, int64_t row0,
+                         int rows, int K, int64_t V, float T, int* sidx, float* sp, float* H,
+                         uint8_t* valid, int* status, cudaStream_t s);
+void launch_fwd_finalize(const float* pm, const float* pl, const float* pg, int stride, int ntiles,
+                         int rows, const float* H, const uint8_t* valid, float T, float* lse,
+                         float* rowloss, cudaStream_t s);
+void launch_loss_reduce(const float* rowloss, int64_t N, const int* n_valid, float T, float* loss,
+                        cudaStream_t s);
+void launch_dh_reduce(const float* part, int splits, size_t split_elems, int rows, int d, void* dh,
+                      cudaStream_t s);
+
+}  // namespace fkl

@@ -1,0 +1,468 @@
+// Persistent tcgen05 GEMM for sm_103a with three epilogues.
+//
+//   C[m, n] = sum_k A(m, k) B(n, k)      bf16 operands, fp32 accumulator in TMEM
+//
+// One CTA per SM (192 threads):
+//   warp 0      one lane issues TMA loads of A and B k-blocks into a STAGES-deep
+//               shared-memory ring (128-byte swizzle), signalling `full` barriers;
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
+//               one lane issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide slice,
+//               committing `empty` barriers to recycle stages and `tfull` barriers
+//               when a tile's accumulator is complete;
+//   warps 2-5   the epilogue: each warp owns 32 TMEM lanes (= 32 output rows),
+//               drains the accumulator with tcgen05.ld and releases it (`tempty`)
+//               so that the MMA of the next tile overlaps this tile's epilogue.
+//
+// Epilogues
+//   EPI_LSE  logits z = h W^T of one row tile x 256 vocabulary columns: online
+//            base-2 max / sum-of-exponentials of z/T per row, plus the teacher
+//            gather sum_k p_k z_{idx_k} over the sorted teacher ids that fall in
+//            the tile.  Writes one (max, sum, gather) triple per row and tile.
+//   EPI_DZ   the same logits recomputed: dz = coef * (2^(z log2e/T - lse log2e) - s)
+//            in bf16, staged per warp in swizzled shared memory and TMA-stored.
+//   EPI_F32  plain fp32 tile, TMA-stored or TMA reduce-added (dh partials, dW).
+//
+// Operand majorness (template): K-major tiles arrive as one TMA box {64, rows};
+// MN-major tiles as boxes {64 (MN), 64 (K)} side by side, 8 KB apart.
+#include <climits>
+#include <cmath>
+
+#include "ptx.cuh"
+
+namespace fkl {
+
+template <int BN>
+struct TileCfg {
+    static constexpr int STAGES = (BN == 128) ? 6 : 4;
+    static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+    static constexpr uint32_t B_BYTES = BN * kBK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t STAGING_BYTES = 4 * 2 * 4096;  // two 32 x 128 B boxes per epilogue warp
+    static constexpr uint32_t BAR_BYTES = 256;
+};
+
+template <int BN, int EPI>
+constexpr size_t smem_total() {
+    using C = TileCfg<BN>;
+    return size_t(C::STAGES) * C::STAGE_BYTES + (EPI == EPI_LSE ? 0 : C::STAGING_BYTES) +
+           C::BAR_BYTES + 1024;
+}
+
+__device__ __forceinline__ void decode_unit(int u, const GemmParams& p, int& m, int& n, int& s) {
+    const int mn = p.m_tiles * p.n_tiles;
+    s = u / mn;
+    const int r = u - s * mn;
+    if (p.m_fastest) {
+        m = r % p.m_tiles;
+        n = r / p.m_tiles;
+    } else {
+        n = r % p.n_tiles;
+        m = r / p.n_tiles;
+    }
+}
+
+__device__ __forceinline__ int kb_begin(const GemmParams& p, int s) {
+    return static_cast<int>((static_cast<long long>(s) * p.kb_total) / p.splits);
+}
+
+// Sorted-teacher cursor of one row: first position whose id is >= v0.
+struct TeacherCursor {
+    const int* ids;
+    const float* probs;
+    int K, pos, next_id;
+    float next_p;
+
+    __device__ __forceinline__ void seek(const int* sidx, const float* sp, int row, bool row_ok, int k,
+                                         int v0) {
+        K = k;
+        ids = sidx + static_cast<size_t>(row_ok ? row : 0) * k;
+        probs = sp + static_cast<size_t>(row_ok ? row : 0) * k;
+        next_id = INT_MAX;
+        next_p = 0.f;
+        pos = k;
+        if (!row_ok) return;
+        int lo = 0, hi = k;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(ids + mid) < v0) lo = mid + 1; else hi = mid;
+        }
+        pos = lo;
+        if (pos < K) {
+            next_id = __ldg(ids + pos);
+            next_p = __ldg(probs + pos);
+        }
+    }
+    __device__ __forceinline__ void advance() {
+        if (++pos < K) {
+            next_id = __ldg(ids + pos);
+            next_p = __ldg(probs + pos);
+        } else {
+            next_id = INT_MAX;
+        }
+    }
+};
+
+// Lane 0 waits, the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <int BN, int A_MN, int B_MN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+    using C = TileCfg<BN>;
+    constexpr int STAGES = C::STAGES;
+    static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "tile width");
+    static_assert(EPI != EPI_DZ || BN % 64 == 0, "dz boxes are 64 columns");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t staging0 = base + STAGES * C::STAGE_BYTES;
+    const uint32_t bar0 = staging0 + (EPI == EPI_LSE ? 0u : C::STAGING_BYTES);
+    uint8_t* gbar = gbase + (bar0 - base);
+    const uint32_t full0 = bar0, empty0 = bar0 + 8u * STAGES, tfull0 = bar0 + 16u * STAGES,
+                   tempty0 = tfull0 + 16u, drain_bar = tempty0 + 16u;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(gbar + 16 * STAGES + 40);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(gbar + 16 * STAGES + 44);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8u * a, 1);
+            mbar_init(tempty0 + 8u * a, 4);
+        }
+        mbar_init(drain_bar, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (EPI != EPI_LSE) tma_prefetch_desc(&tmOut);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(s_tmem), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const int units = p.m_tiles * p.n_tiles * p.splits;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int m, n, s;
+                decode_unit(u, p, m, n, s);
+                const int kb0 = kb_begin(p, s), kb1 = kb_begin(p, s + 1);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, s_abort, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * C::STAGE_BYTES, sb = sa + C::A_BYTES;
+                    const uint32_t fb = full0 + 8u * stage;
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    if (A_MN == 0) {
+                        tma_load_2d(sa, &tmA, fb, kb * kBK, m * kBM);
+                    } else {
+                        tma_load_2d(sa, &tmA, fb, m * kBM, kb * kBK);
+                        tma_load_2d(sa + 8192u, &tmA, fb, m * kBM + 64, kb * kBK);
+                    }
+                    if (B_MN == 0) {
+                        tma_load_2d(sb, &tmB, fb, kb * kBK, n * BN);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(sb + 8192u * j, &tmB, fb, n * BN + 64 * j, kb * kBK);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {  // let the copies already in flight land before the CTA exits
+                const long long first = issued > STAGES ? issued - STAGES : 0;
+                for (long long i = first; i < issued; ++i)
+                    mbar_wait_drain(full0 + 8u * static_cast<uint32_t>(i % STAGES),
+                                    static_cast<uint32_t>((i / STAGES) & 1));
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = umma_idesc_bf16(kBM, BN, A_MN, B_MN);
+            int stage = 0, tc = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++tc) {
+                int m, n, s;
+                decode_unit(u, p, m, n, s);
+                const int kb0 = kb_begin(p, s), kb1 = kb_begin(p, s + 1);
+                const int acc = tc & 1;
+                const uint32_t aph = (tc >> 1) & 1;
+                if (!mbar_wait(tempty0 + 8u * acc, aph ^ 1u, s_abort, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * 256);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(full0 + 8u * stage, phase, s_abort, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + stage * C::STAGE_BYTES, sb = sa + C::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * kk, 8192u, 1024u)
+                                                 : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048u * kk, 8192u, 1024u)
+                                                 : smem_desc_sw128(sb + 32u * kk, 16u, 1024u);
+                        umma_bf16(dt, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(empty0 + 8u * stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull0 + 8u * acc);
+            }
+            if (!ok) {  // no MMA may still be running when TMEM is released
+                umma_commit(drain_bar);
+                mbar_wait_drain(drain_bar, 0);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        uint32_t box = 0;
+        int tc = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++tc) {
+            int m, n, s;
+            decode_unit(u, p, m, n, s);
+            const int acc = tc & 1;
+            const uint32_t aph = (tc >> 1) & 1;
+            const int row = m * kBM + q * 32 + lane;
+            const bool row_ok = row < p.M;
+            const uint32_t tt = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                static_cast<uint32_t>(acc * 256);
+
+            if constexpr (EPI == EPI_LSE) {
+                const int v0 = n * BN;
+                TeacherCursor cur;
+                cur.seek(p.sidx, p.sp, row, row_ok, p.K, v0);
+                if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
+                tc_fence_after();
+                float mrun = -INFINITY, lrun = 0.f, g = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int col0 = v0 + c * 32;
+                    if (col0 >= p.Ncols) break;
+                    float z[32];
+                    __syncwarp();
+                    tmem_ld32(tt + c * 32, z);
+                    while (cur.next_id < col0 + 32) {
+                        g += cur.next_p * select32(z, cur.next_id - col0);
+                        cur.advance();
+                    }
+                    const int nv = p.Ncols - col0;
+                    float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        z[j] = (j < nv) ? z[j] * p.scale2 : -INFINITY;
+                        z[j + 1] = (j + 1 < nv) ? z[j + 1] * p.scale2 : -INFINITY;
+                        cm0 = fmaxf(cm0, z[j]);
+                        cm1 = fmaxf(cm1, z[j + 1]);
+                    }
+                    const float mnew = fmaxf(mrun, fmaxf(cm0, cm1));
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        s0 += ex2_approx(z[j] - mnew);
+                        s1 += ex2_approx(z[j + 1] - mnew);
+                        s2 += ex2_approx(z[j + 2] - mnew);
+                        s3 += ex2_approx(z[j + 3] - mnew);
+                    }
+                    lrun = lrun * ex2_approx(mrun - mnew) + ((s0 + s1) + (s2 + s3));
+                    mrun = mnew;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+                if (row_ok) {
+                    const size_t o = static_cast<size_t>(n) * p.part_stride + row;
+                    p.part_m[o] = mrun;
+                    p.part_l[o] = lrun;
+                    p.part_g[o] = g;
+                }
+            } else if constexpr (EPI == EPI_DZ) {
+                const int v0 = n * BN;
+                TeacherCursor cur;
+                cur.seek(p.sidx, p.sp, row, row_ok, p.K, v0);
+                float lse2 = 0.f, coef = 0.f;
+                if (row_ok) {
+                    lse2 = p.lse[row] * 1.4426950408889634f;
+                    const int nvalid = *p.n_valid;
+                    if (p.valid[row] && nvalid > 0)
+                        coef = p.T * (p.grad ? *p.grad : 1.f) / static_cast<float>(nvalid);
+                }
+                if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
+                tc_fence_after();
+                const int out_row = m * kBM + q * 32;
+#pragma unroll 1
+                for (int c2 = 0; c2 < BN / 64; ++c2) {
+                    const int col0 = v0 + c2 * 64;
+                    if (col0 >= p.Ncols) break;
+                    const uint32_t buf = staging0 + static_cast<uint32_t>(q * 2 + (box & 1)) * 4096u;
+                    if (lane == 0) bulk_wait_read_le1();
+                    __syncwarp();
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int cc = col0 + hh * 32;
+                        float z[32];
+                        __syncwarp();
+                        tmem_ld32(tt + c2 * 64 + hh * 32, z);
+                        const int nv = p.Ncols - cc;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            z[j] = (j < nv) ? ex2_approx(z[j] * p.scale2 - lse2) : 0.f;
+                        while (cur.next_id < cc + 32) {
+                            const int off = cur.next_id - cc;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) z[j] -= (j == off) ? cur.next_p : 0.f;
+                            cur.advance();
+                        }
+                        uint32_t w[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(coef * z[2 * j], coef * z[2 * j + 1]);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            st_shared_v4(buf + lane * 128u + ((static_cast<uint32_t>(hh * 4 + k) ^ (lane & 7u)) << 4),
+                                         w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && out_row < p.M) {
+                        tma_store_2d(&tmOut, buf, col0, out_row);
+                        bulk_commit();
+                    }
+                    ++box;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+            } else {
+                if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
+                tc_fence_after();
+                const int out_row = s * p.split_row_stride + m * kBM + q * 32;
+                const bool rows_ok = m * kBM + q * 32 < p.M;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int col0 = n * BN + c * 32;
+                    if (col0 >= p.Ncols) break;
+                    const uint32_t buf = staging0 + static_cast<uint32_t>(q * 2 + (box & 1)) * 4096u;
+                    if (lane == 0) bulk_wait_read_le1();
+                    __syncwarp();
+                    float z[32];
+                    tmem_ld32(tt + c * 32, z);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_shared_v4(buf + lane * 128u + ((static_cast<uint32_t>(k) ^ (lane & 7u)) << 4),
+                                     __float_as_uint(z[4 * k]), __float_as_uint(z[4 * k + 1]),
+                                     __float_as_uint(z[4 * k + 2]), __float_as_uint(z[4 * k + 3]));
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && rows_ok) {
+                        if (p.reduce) tma_reduce_add_2d(&tmOut, buf, col0, out_row);
+                        else tma_store_2d(&tmOut, buf, col0, out_row);
+                        bulk_commit();
+                    }
+                    ++box;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+            }
+        }
+        if (EPI != EPI_LSE && lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ---------------------------------------------------------------- host dispatch
+int gemm_stages(int bn) { return bn == 128 ? TileCfg<128>::STAGES : TileCfg<256>::STAGES; }
+
+size_t gemm_smem_bytes(int bn, int epi) {
+    if (bn == 256) return epi == EPI_LSE ? smem_total<256, EPI_LSE>() : smem_total<256, EPI_F32>();
+    if (bn == 192) return epi == EPI_LSE ? smem_total<192, EPI_LSE>() : smem_total<192, EPI_F32>();
+    return epi == EPI_LSE ? smem_total<128, EPI_LSE>() : smem_total<128, EPI_F32>();
+}
+
+template <int BN, int A_MN, int B_MN, int EPI>
+static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmOut,
+                              const GemmParams& p, int grid, cudaStream_t stream) {
+    constexpr size_t smem = smem_total<BN, EPI>();
+    static_assert(smem <= 232448, "shared memory per CTA");
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, A_MN, B_MN, EPI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    gemm_kernel<BN, A_MN, B_MN, EPI><<<grid, kThreads, smem, stream>>>(tmA, tmB, tmOut, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& tmA,
+                        const CUtensorMap& tmB, const CUtensorMap& tmOut, const GemmParams& p,
+                        int grid, cudaStream_t stream) {
+    if (epi == EPI_LSE) {
+        if (bn == 256 && a_mn == 0 && b_mn == 0)
+            return launch_one<256, 0, 0, EPI_LSE>(tmA, tmB, tmOut, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (epi == EPI_DZ) {
+        if (bn == 256 && a_mn == 0 && b_mn == 0)
+            return launch_one<256, 0, 0, EPI_DZ>(tmA, tmB, tmOut, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+#define FKL_F32_CASE(BN_, A_, B_)                                                       \
+    if (bn == BN_ && a_mn == A_ && b_mn == B_)                                          \
+        return launch_one<BN_, A_, B_, EPI_F32>(tmA, tmB, tmOut, p, grid, stream);
+    FKL_F32_CASE(256, 0, 0) FKL_F32_CASE(256, 0, 1) FKL_F32_CASE(256, 1, 0) FKL_F32_CASE(256, 1, 1)
+    FKL_F32_CASE(192, 0, 0) FKL_F32_CASE(192, 0, 1) FKL_F32_CASE(192, 1, 0) FKL_F32_CASE(192, 1, 1)
+    FKL_F32_CASE(128, 0, 0) FKL_F32_CASE(128, 0, 1) FKL_F32_CASE(128, 1, 0) FKL_F32_CASE(128, 1, 1)
+#undef FKL_F32_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fkl

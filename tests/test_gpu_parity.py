@@ -1,0 +1,135 @@
+"""Fused CUDA path against the fp64 oracle, element by element, on sizes the
+oracle finishes in seconds (several tiles, ragged tails in N, d and V, several
+chunks), plus edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lm_head_kl_fkl_b300 import api, synth
+from tests.gpu_helpers import (TOL_GRAD_REL_L2, TOL_LOSS_REL, TOL_LSE_ABS, oracle_inputs, rel_l2,
+                               run_fused, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(x, out, grad=1.0, tol_scale=1.0):
+    h, W = oracle_inputs(x)
+    ref = oracle.forward(h, W, x["idx"], x["t"], x["mask"], x["T"])
+    g = oracle.backward(h, W, x["idx"], x["t"], x["mask"], x["T"], grad_loss=grad)
+    if ref["n_valid"] > 0:
+        assert abs(out["loss"] - ref["loss"]) <= TOL_LOSS_REL * abs(ref["loss"]), (out["loss"], ref["loss"])
+    else:
+        assert out["loss"] == 0.0
+    assert np.abs(out["lse"] - ref["lse"]).max() <= TOL_LSE_ABS
+    if ref["n_valid"] > 0:
+        assert rel_l2(out["dh"], g["dh"]) <= TOL_GRAD_REL_L2 * tol_scale, rel_l2(out["dh"], g["dh"])
+        assert rel_l2(out["dW"], g["dW"]) <= TOL_GRAD_REL_L2 * tol_scale, rel_l2(out["dW"], g["dW"])
+    else:
+        assert not out["dh"].any() and not out["dW"].any()
+    return ref, g
+
+
+SHAPES = [
+    # N, d, V, K, T, index, chunk
+    (300, 136, 1000, 16, 1.5, "uniform", 128),      # 3 chunks, ragged rows; d not a multiple of 64
+    (257, 64, 1001, 8, 1.0, "uniform", 0),           # V odd: dz row stride padded; one ragged row tile
+    (640, 256, 4096, 100, 2.0, "zipf1.1", 256),      # many teacher hits in the first vocab tiles
+    (130, 384, 2304, 32, 0.5, "half-student", 0),    # teacher overlaps the student's top-K
+    (96, 200, 777, 5, 1.0, "uniform", 0),            # everything ragged, N below one tile
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "N{}_d{}_V{}_K{}".format(*s[:4]))
+def test_parity_small(shape):
+    N, d, V, K, T, index, chunk = shape
+    x = synth.make_inputs(N, d, V, K, T, 0.05, index, seed=1000 + N)
+    out = run_fused(to_device(x), chunk=chunk)
+    _check(x, out)
+
+
+def test_parity_tiny_config():
+    x = synth.config_inputs(0)
+    out = run_fused(to_device(x))
+    _check(x, out)
+
+
+def test_upstream_gradient_scales_dz():
+    x = synth.make_inputs(200, 128, 600, 12, 1.0, 0.05, "uniform", seed=77)
+    out = run_fused(to_device(x), grad=-2.5)
+    _check(x, out, grad=-2.5)
+
+
+def test_k1_single_teacher_entry():
+    x = synth.make_inputs(150, 64, 512, 1, 1.0, 0.05, "uniform", seed=78)
+    _check(x, run_fused(to_device(x)))
+
+
+def test_all_rows_masked():
+    x = synth.make_inputs(64, 64, 300, 4, 1.0, 0.0, "uniform", seed=79, n_pad=64)
+    out = run_fused(to_device(x))
+    _check(x, out)
+
+
+def test_no_mask_and_minus_inf_teacher_logits():
+    x = synth.make_inputs(70, 64, 400, 6, 1.0, 0.0, "uniform", seed=80)
+    x["mask"] = None
+    x["t"][3, 2:] = -np.inf       # partial: p = 0 on those entries
+    x["t"][5, :] = -np.inf        # whole row: not a valid token
+    out = run_fused(to_device(x))
+    _check(x, out)
+
+
+def test_single_row():
+    x = synth.make_inputs(1, 64, 256, 4, 1.0, 0.0, "uniform", seed=81)
+    _check(x, run_fused(to_device(x)))
+
+
+def test_loss_and_lse_bitwise_chunk_invariant():
+    x = synth.make_inputs(1000, 128, 2000, 20, 1.0, 0.05, "uniform", seed=82)
+    xd = to_device(x)
+    outs = []
+    for chunk in (128, 384, 1024, 0):
+        loss, lse = api.forward(xd["h"], xd["W"], xd["idx"], xd["t"], xd["mask"], xd["T"], chunk)
+        outs.append((loss.item(), lse.cpu().numpy()))
+    for loss, lse in outs[1:]:
+        assert loss == outs[0][0]
+        assert np.array_equal(lse, outs[0][1])
+
+
+def test_backward_deterministic():
+    x = synth.make_inputs(600, 128, 3000, 16, 1.0, 0.05, "uniform", seed=83)
+    xd = to_device(x)
+    a = run_fused(xd, chunk=256)
+    b = run_fused(xd, chunk=256)
+    assert np.array_equal(a["dh"], b["dh"]) and np.array_equal(a["dW"], b["dW"])
+
+
+def test_out_of_range_teacher_index_sets_status():
+    x = synth.make_inputs(64, 64, 300, 4, 1.0, 0.0, "uniform", seed=84)
+    x["idx"][10, 1] = 300  # == V
+    xd = to_device(x)
+    ws = api.alloc_workspace(64, 64, 300, 4)
+    api.forward(xd["h"], xd["W"], xd["idx"], xd["t"], xd["mask"], 1.0, ws=ws)
+    assert api.get_status(ws) == 3
+    x["idx"][10, 1] = 0 if 0 not in x["idx"][10] else 299
+    xd = to_device(x)
+    api.forward(xd["h"], xd["W"], xd["idx"], xd["t"], xd["mask"], 1.0, ws=ws)
+    assert api.get_status(ws) == 0
+
+
+def test_autograd_loss_matches_oracle():
+    x = synth.make_inputs(256, 128, 1024, 16, 2.0, 0.05, "uniform", seed=85)
+    xd = to_device(x)
+    h = xd["h"].clone().requires_grad_(True)
+    W = xd["W"].clone().requires_grad_(True)
+    loss = api.fkl_loss(h, W, xd["idx"], xd["t"], xd["mask"], 2.0)
+    (3.0 * loss).backward()
+    out = dict(loss=loss.item(), lse=None)
+    hh, WW = oracle_inputs(x)
+    ref = oracle.forward(hh, WW, x["idx"], x["t"], x["mask"], 2.0)
+    g = oracle.backward(hh, WW, x["idx"], x["t"], x["mask"], 2.0, grad_loss=3.0)
+    assert abs(out["loss"] - ref["loss"]) <= TOL_LOSS_REL * abs(ref["loss"])
+    assert rel_l2(h.grad.double().cpu().numpy(), g["dh"]) <= TOL_GRAD_REL_L2
+    assert rel_l2(W.grad.double().cpu().numpy(), g["dW"]) <= TOL_GRAD_REL_L2
+    assert torch.isfinite(h.grad).all()
