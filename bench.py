@@ -152,10 +152,17 @@ def cpu_baseline(x, budget_s=12.0, max_rows=1024):
                       f"backward, {dt:.1f} s"}
 
 
-def workload(cfg):
+def workload(cfg, shape=None):
+    """Inputs of a named workload, or of a custom (N, d, V, K) with that workload's generators."""
+    import dataclasses
     from lm_head_kl_fkl_b300 import synth
-    x = synth.config_inputs(cfg)
     c = synth.CONFIGS[cfg]
+    if shape is None:
+        return synth.config_inputs(cfg), c
+    N, d, V, K = shape
+    c = dataclasses.replace(c, name=f"{c.name}-shape-N{N}-d{d}-V{V}-K{K}", N=N, d=d, V=V, K=K)
+    x = synth.make_inputs(N, d, V, K, c.T, c.pad_frac, c.index, synth.config_seed(cfg))
+    x["name"] = c.name
     return x, c
 
 
@@ -170,7 +177,7 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return 0
-    x, c = workload(args.config)
+    x, c = workload(args.config, args.shape)
     from lm_head_kl_fkl_b300 import synth
     Wf = synth.bf16_bits_to_f64(x["W"])
     rng = np.random.default_rng(2)
@@ -206,7 +213,7 @@ def run_fused(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    x, c = workload(args.config)
+    x, c = workload(args.config, args.shape)
     N, d, V, K, T = c.N, c.d, c.V, c.K, c.T
     stream = torch.cuda.current_stream(dev)
 
@@ -360,6 +367,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--shape", type=lambda s: tuple(int(v) for v in s.split(",")), default=None,
+                    help="N,d,V,K: a smaller case of the chosen workload (profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "fused":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
