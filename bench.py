@@ -92,7 +92,7 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in (self.out or "").strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
@@ -101,6 +101,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
             except ValueError:
                 continue
             for n, v in zip(names, parts[5:9]):
@@ -109,7 +110,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "power_w": statistics.median(pw) if pw else None, "reasons": sorted(reasons)}
 
 
 def threads_used():

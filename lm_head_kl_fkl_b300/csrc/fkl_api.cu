@@ -17,6 +17,7 @@
 #include <cstdarg>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -179,11 +180,14 @@ int pick_bn(int d) {
     return best;
 }
 
+// Split count of the dh GEMM over V: the smallest S whose units (pair tiles x S)
+// fill the CTA pairs' waves best (each extra split costs C * d * 4 bytes).
 int pick_splits(int m_tiles, int n_tiles, int64_t kb_total) {
+    const int pairs = kPlanSMs / 2;
     auto eff = [&](int s) {
         const int64_t units = int64_t(m_tiles) * n_tiles * s;
-        const int64_t waves = cdiv(units, kPlanSMs);
-        return double(units) / double(waves * kPlanSMs);
+        const int64_t waves = cdiv(units, pairs);
+        return double(units) / double(waves * pairs);
     };
     int best = 1;
     for (int s = 2; s <= 8; ++s) {
@@ -217,8 +221,12 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
     P.n_chunks = cdiv(N, P.Cc);
     P.nt_v = static_cast<int>(cdiv(V, kVocabTile));
     P.bn_d = pick_bn(d);
+    if (const char* e = getenv("FKL_BN_D")) {  // tile-width override for tuning sweeps
+        const int v = atoi(e);
+        if (v == 256 || v == 192 || v == 128) P.bn_d = v;
+    }
     P.nt_d = static_cast<int>(cdiv(d, P.bn_d));
-    P.splits = pick_splits(static_cast<int>(cdiv(P.Cc, kBM)), P.nt_d, cdiv(V, kBK));
+    P.splits = pick_splits(static_cast<int>(cdiv(P.Cc, kPairRows)), P.nt_d, cdiv(V, kBK));
     P.Vs = cdiv(V, 8) * 8;
     size_t off = 256;  // header: status word, N_valid
     P.o_sidx = off;
@@ -266,12 +274,10 @@ fkl_status device_ready() {
 
 fkl_status run_gemm(int kind, int bn, int a_mn, int b_mn, int epi, const CUtensorMap& a, const CUtensorMap& b,
                     const CUtensorMap& o, const GemmParams& p, double flop, cudaStream_t s) {
-    const int64_t units = int64_t(p.m_tiles) * p.n_tiles * p.splits;
-    const int grid = static_cast<int>(std::min<int64_t>(units, device_info().sms));
     cudaError_t e;
     {
         LaunchScope ls(kind, flop, s);
-        e = launch_gemm(bn, a_mn, b_mn, epi, a, b, o, p, grid, s);
+        e = launch_gemm(bn, a_mn, b_mn, epi, a, b, o, p, device_info().sms / 2, s);
     }
     if (e != cudaSuccess) return fail(FKL_ERR_CUDA, "%s launch: %s", kKindNames[kind], cudaGetErrorString(e));
     return FKL_OK;
@@ -355,8 +361,8 @@ fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const f
     const int sms = device_info().sms;
     FKL_SMALL(KK_COUNT_VALID, launch_count_valid(tlogit, mask, N, K, n_valid, sms * 4, s));
 
-    CUtensorMap tmW;
-    FKL_TMAP(tmW, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 256);
+    CUtensorMap tmW;  // B of the logit GEMM: each CTA of a pair loads 128 of the tile's 256 vocab rows
+    FKL_TMAP(tmW, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, kVocabTile / 2);
     for (int64_t c = 0; c < P.n_chunks; ++c) {
         const int64_t row0 = c * P.Cc;
         const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
@@ -366,7 +372,7 @@ fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const f
         FKL_TMAP(tmH, BF16, static_cast<const char*>(h) + size_t(row0) * d * 2, uint64_t(d), uint64_t(rows),
                  uint64_t(d) * 2, 64, 128);
         GemmParams p{};
-        p.m_tiles = static_cast<int>(cdiv(rows, kBM));
+        p.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
         p.n_tiles = P.nt_v;
         p.splits = 1;
         p.kb_total = static_cast<int>(cdiv(d, kBK));
@@ -422,7 +428,7 @@ fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const 
     FKL_SMALL(KK_COUNT_VALID, launch_count_valid(tlogit, mask, N, K, n_valid, sms * 4, s));
 
     CUtensorMap tmW_k, tmW_mn, tmDW;
-    FKL_TMAP(tmW_k, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 256);
+    FKL_TMAP(tmW_k, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, kVocabTile / 2);
     FKL_TMAP(tmW_mn, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 64);
     FKL_TMAP(tmDW, F32, dW, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32);
     for (int64_t c = 0; c < P.n_chunks; ++c) {
@@ -442,7 +448,7 @@ fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const 
 
         // dz = T g (q - s) / N_valid for this chunk's rows, bf16 [rows][V]
         GemmParams p{};
-        p.m_tiles = static_cast<int>(cdiv(rows, kBM));
+        p.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
         p.n_tiles = P.nt_v;
         p.splits = 1;
         p.kb_total = static_cast<int>(cdiv(d, kBK));
@@ -463,11 +469,11 @@ fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const 
 
         // dh partials: [split][rows][d] = dz[:, split's V range] W[split's V range, :]
         GemmParams q{};
-        q.m_tiles = static_cast<int>(cdiv(rows, kBM));
+        q.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
         q.n_tiles = P.nt_d;
         q.splits = P.splits;
         q.kb_total = static_cast<int>(cdiv(V, kBK));
-        q.m_fastest = 1;
+        q.m_fastest = 0;  // pairs in flight cover every d tile of a few row tiles: dz is read once
         q.M = rows;
         q.Ncols = d;
         q.status = status;
@@ -480,7 +486,7 @@ fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const 
 
         // dW (+)= dz^T h_chunk, one owner per output tile, chunks in order
         GemmParams r{};
-        r.m_tiles = static_cast<int>(cdiv(V, kBM));
+        r.m_tiles = static_cast<int>(cdiv(V, kPairRows));
         r.n_tiles = P.nt_d;
         r.splits = 1;
         r.kb_total = static_cast<int>(cdiv(rows, kBK));
@@ -553,11 +559,11 @@ fkl_status fkl_selftest_gemm(const void* A, const void* B, float* C, int M, int 
     CUtensorMap ta, tb, tc;
     if (a_mn == 0) FKL_TMAP(ta, BF16, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, 64, 128);
     else FKL_TMAP(ta, BF16, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, 64);
-    if (b_mn == 0) FKL_TMAP(tb, BF16, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, 64, uint32_t(bn));
+    if (b_mn == 0) FKL_TMAP(tb, BF16, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, 64, uint32_t(bn / 2));
     else FKL_TMAP(tb, BF16, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, 64);
     FKL_TMAP(tc, F32, C, uint64_t(N), uint64_t(M), uint64_t(N) * 4, 32, 32);
     GemmParams p{};
-    p.m_tiles = static_cast<int>(cdiv(M, kBM));
+    p.m_tiles = static_cast<int>(cdiv(M, kPairRows));
     p.n_tiles = static_cast<int>(cdiv(N, bn));
     p.splits = 1;
     p.kb_total = static_cast<int>(cdiv(K, kBK));

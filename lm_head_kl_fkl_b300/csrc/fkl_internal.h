@@ -10,7 +10,8 @@
 
 namespace fkl {
 
-constexpr int kBM = 128;          // rows of one UMMA tile (TMEM lanes)
+constexpr int kBM = 128;          // rows of a tile held by one CTA (its TMEM lanes)
+constexpr int kPairRows = 256;    // rows of the tile a CTA pair computes
 constexpr int kBK = 64;           // K elements per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kVocabTile = 256;   // vocabulary columns per tile in the logit GEMMs
 constexpr int kThreads = 192;     // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
@@ -35,7 +36,7 @@ enum KernelKind {
 enum Epilogue { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2 };
 
 // Parameters of one persistent GEMM launch.  The unit space is
-// m_tiles x n_tiles x splits; unit u maps to (m, n, s) with s slowest and either
+// m_tiles (of 256 rows) x n_tiles (of BN columns) x splits; unit u maps to (m, n, s) with s slowest and either
 // m (m_fastest = 1) or n fastest; split s covers k-blocks
 // [s * kb_total / splits, (s + 1) * kb_total / splits).
 struct GemmParams {
@@ -63,11 +64,12 @@ struct GemmParams {
 };
 
 // Launch helpers implemented in gemm_tc.cu.  Return cudaSuccess or the launch error.
+// Launches on at most `max_pairs` CTA pairs (clusters of 2), fewer if the unit
+// space is smaller or fewer pairs can be resident.
 cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& tmA,
                         const CUtensorMap& tmB, const CUtensorMap& tmOut, const GemmParams& p,
-                        int grid, cudaStream_t stream);
-size_t gemm_smem_bytes(int bn, int epi);
-int gemm_stages(int bn);
+                        int max_pairs, cudaStream_t stream);
+size_t gemm_smem_bytes(int bn, int b_mn, int epi);
 
 // Small kernels implemented in aux_kernels.cu.
 void launch_count_valid(const float* tlogit, const uint8_t* mask, int64_t N, int K, int* n_valid,

@@ -1,23 +1,31 @@
-// Persistent tcgen05 GEMM for sm_103a with three epilogues.
+// Persistent 2-SM tcgen05 GEMM for sm_103a with three epilogues.
 //
 //   C[m, n] = sum_k A(m, k) B(n, k)      bf16 operands, fp32 accumulator in TMEM
 //
-// One CTA per SM (192 threads):
-//   warp 0      one lane issues TMA loads of A and B k-blocks into a STAGES-deep
-//               shared-memory ring (128-byte swizzle), signalling `full` barriers;
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
-//               one lane issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide slice,
-//               committing `empty` barriers to recycle stages and `tfull` barriers
-//               when a tile's accumulator is complete;
-//   warps 2-5   the epilogue: each warp owns 32 TMEM lanes (= 32 output rows),
-//               drains the accumulator with tcgen05.ld and releases it (`tempty`)
-//               so that the MMA of the next tile overlaps this tile's epilogue.
+// CTAs run in pairs (a cluster of 2).  A pair owns one 256 x BN output tile at a
+// time: CTA rank r holds rows [128 r, 128 r + 128) of A and columns
+// [r BN/2, (r+1) BN/2) of B in its own shared memory, and the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256, N = BN, K = 16), which reads both CTAs'
+// operands and leaves rows [128 r, 128 r + 128) of the tile in CTA r's TMEM.
+// Per SM this halves the B operand's L2->SMEM traffic and shared-memory reads
+// against a one-SM 128 x BN tile, and leaves room for a deeper TMA ring.
+//
+// Roles, in each CTA of the pair (192 threads, one CTA per SM):
+//   warp 0      one lane issues the CTA's TMA loads of A and B k-blocks into a
+//               STAGES-deep ring (128-byte swizzle); both CTAs' copies complete
+//               on the even CTA's `full` barrier, which the even CTA arms with
+//               the byte count of the pair;
+//   warp 1      allocates 512 TMEM columns (two accumulators) for the pair; in
+//               the even CTA one lane issues the MMAs, commits `empty` (stage
+//               reusable) and `tfull` (accumulator complete) to both CTAs;
+//   warps 2-5   the epilogue: each warp drains its 32 TMEM lanes (= 32 output
+//               rows) with tcgen05.ld and reports the buffer free on the even
+//               CTA's `tempty` barrier, so the next tile's MMAs overlap it.
 //
 // Epilogues
-//   EPI_LSE  logits z = h W^T of one row tile x 256 vocabulary columns: online
-//            base-2 max / sum-of-exponentials of z/T per row, plus the teacher
-//            gather sum_k p_k z_{idx_k} over the sorted teacher ids that fall in
-//            the tile.  Writes one (max, sum, gather) triple per row and tile.
+//   EPI_LSE  logits of a row pair-tile x 256 vocabulary columns: online base-2
+//            max / sum of 2^(z log2e / T) per row plus the teacher gather
+//            sum_k p_k z_{idx_k}; one (max, sum, gather) triple per row and tile.
 //   EPI_DZ   the same logits recomputed: dz = coef * (2^(z log2e/T - lse log2e) - s)
 //            in bf16, staged per warp in swizzled shared memory and TMA-stored.
 //   EPI_F32  plain fp32 tile, TMA-stored or TMA reduce-added (dh partials, dW).
@@ -31,22 +39,19 @@
 
 namespace fkl {
 
-template <int BN>
-struct TileCfg {
-    static constexpr int STAGES = (BN == 128) ? 6 : 4;
-    static constexpr uint32_t A_BYTES = kBM * kBK * 2;
-    static constexpr uint32_t B_BYTES = BN * kBK * 2;
+template <int BN, int B_MN, int EPI>
+struct PairCfg {
+    static constexpr int BNH = BN / 2;                     // B columns held by one CTA
+    static constexpr uint32_t A_BYTES = kBM * kBK * 2;     // 128 rows x 64 k, bf16
+    static constexpr int B_BOXES = B_MN ? (BNH + 63) / 64 : 1;
+    static constexpr uint32_t B_BYTES = B_MN ? B_BOXES * 8192u : static_cast<uint32_t>(BNH) * 128u;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t STAGING_BYTES = 4 * 2 * 4096;  // two 32 x 128 B boxes per epilogue warp
+    static constexpr uint32_t STAGING_BYTES = EPI == EPI_LSE ? 0u : 4u * 2u * 4096u;
+    static constexpr uint32_t RING_BUDGET = 196608u + (EPI == EPI_LSE ? 32768u : 0u);
+    static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) > 8 ? 8 : (RING_BUDGET / STAGE_BYTES);
     static constexpr uint32_t BAR_BYTES = 256;
+    static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + STAGING_BYTES + BAR_BYTES + 1024;
 };
-
-template <int BN, int EPI>
-constexpr size_t smem_total() {
-    using C = TileCfg<BN>;
-    return size_t(C::STAGES) * C::STAGE_BYTES + (EPI == EPI_LSE ? 0 : C::STAGING_BYTES) +
-           C::BAR_BYTES + 1024;
-}
 
 __device__ __forceinline__ void decode_unit(int u, const GemmParams& p, int& m, int& n, int& s) {
     const int mn = p.m_tiles * p.n_tiles;
@@ -111,20 +116,22 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 template <int BN, int A_MN, int B_MN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-    using C = TileCfg<BN>;
+    using C = PairCfg<BN, B_MN, EPI>;
     constexpr int STAGES = C::STAGES;
-    static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "tile width");
+    constexpr int BNH = C::BNH;
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
     static_assert(EPI != EPI_DZ || BN % 64 == 0, "dz boxes are 64 columns");
+    static_assert(B_MN || BNH <= 256, "K-major B box height");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t staging0 = base + STAGES * C::STAGE_BYTES;
-    const uint32_t bar0 = staging0 + (EPI == EPI_LSE ? 0u : C::STAGING_BYTES);
+    const uint32_t bar0 = staging0 + C::STAGING_BYTES;
     uint8_t* gbar = gbase + (bar0 - base);
     const uint32_t full0 = bar0, empty0 = bar0 + 8u * STAGES, tfull0 = bar0 + 16u * STAGES,
                    tempty0 = tfull0 + 16u, drain_bar = tempty0 + 16u;
@@ -132,6 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* s_abort = reinterpret_cast<volatile int*>(gbar + 16 * STAGES + 44);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8u * s, 1);
@@ -139,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull0 + 8u * a, 1);
-            mbar_init(tempty0 + 8u * a, 4);
+            mbar_init(tempty0 + 8u * a, 8);  // 4 epilogue warps in each CTA of the pair
         }
         mbar_init(drain_bar, 1);
         *s_abort = 0;
@@ -149,46 +158,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (EPI != EPI_LSE) tma_prefetch_desc(&tmOut);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(s_tmem), 512);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_u32(s_tmem), 512);
+        tmem_relinquish_pair();
     }
+    // barriers of both CTAs initialised and TMEM allocated before any peer traffic
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
     const int units = p.m_tiles * p.n_tiles * p.splits;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            const uint32_t full_leader = mapa_shared(full0, 0);
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            for (int u = pair; u < units && ok; u += npairs) {
                 int m, n, s;
                 decode_unit(u, p, m, n, s);
                 const int kb0 = kb_begin(p, s), kb1 = kb_begin(p, s + 1);
+                const int arow = m * 2 * kBM + static_cast<int>(rank) * kBM;
+                const int bcol = n * BN + static_cast<int>(rank) * BNH;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, s_abort, p.status)) {
                         ok = false;
                         break;
                     }
                     const uint32_t sa = base + stage * C::STAGE_BYTES, sb = sa + C::A_BYTES;
-                    const uint32_t fb = full0 + 8u * stage;
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t fb = full_leader + 8u * stage;
+                    if (leader) mbar_arrive_expect_tx(full0 + 8u * stage, 2u * C::STAGE_BYTES);
                     if (A_MN == 0) {
-                        tma_load_2d(sa, &tmA, fb, kb * kBK, m * kBM);
+                        tma_load_2d_pair(sa, &tmA, fb, kb * kBK, arow);
                     } else {
-                        tma_load_2d(sa, &tmA, fb, m * kBM, kb * kBK);
-                        tma_load_2d(sa + 8192u, &tmA, fb, m * kBM + 64, kb * kBK);
+                        tma_load_2d_pair(sa, &tmA, fb, arow, kb * kBK);
+                        tma_load_2d_pair(sa + 8192u, &tmA, fb, arow + 64, kb * kBK);
                     }
                     if (B_MN == 0) {
-                        tma_load_2d(sb, &tmB, fb, kb * kBK, n * BN);
+                        tma_load_2d_pair(sb, &tmB, fb, kb * kBK, bcol);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(sb + 8192u * j, &tmB, fb, n * BN + 64 * j, kb * kBK);
+                        for (int j = 0; j < C::B_BOXES; ++j)
+                            tma_load_2d_pair(sb + 8192u * j, &tmB, fb, bcol + 64 * j, kb * kBK);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -197,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok) {  // let the copies already in flight land before the CTA exits
+            if (!ok && leader) {  // let the pair's copies already in flight land
                 const long long first = issued > STAGES ? issued - STAGES : 0;
                 for (long long i = first; i < issued; ++i)
                     mbar_wait_drain(full0 + 8u * static_cast<uint32_t>(i % STAGES),
@@ -205,13 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC = umma_idesc_bf16(kBM, BN, A_MN, B_MN);
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && leader) {
+            constexpr uint32_t IDESC = umma_idesc_bf16(2 * kBM, BN, A_MN, B_MN);
             int stage = 0, tc = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++tc) {
+            for (int u = pair; u < units && ok; u += npairs, ++tc) {
                 int m, n, s;
                 decode_unit(u, p, m, n, s);
                 const int kb0 = kb_begin(p, s), kb1 = kb_begin(p, s + 1);
@@ -236,33 +250,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
                         const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048u * kk, 8192u, 1024u)
                                                  : smem_desc_sw128(sb + 32u * kk, 16u, 1024u);
-                        umma_bf16(dt, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_pair(dt, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(empty0 + 8u * stage);
+                    umma_commit_pair(empty0 + 8u * stage);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull0 + 8u * acc);
+                umma_commit_pair(tfull0 + 8u * acc);
             }
             if (!ok) {  // no MMA may still be running when TMEM is released
-                umma_commit(drain_bar);
+                umma_commit_pair(drain_bar);
                 mbar_wait_drain(drain_bar, 0);
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const uint32_t tempty_leader = mapa_shared(tempty0, 0);
         uint32_t box = 0;
         int tc = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x, ++tc) {
+        for (int u = pair; u < units; u += npairs, ++tc) {
             int m, n, s;
             decode_unit(u, p, m, n, s);
             const int acc = tc & 1;
             const uint32_t aph = (tc >> 1) & 1;
-            const int row = m * kBM + q * 32 + lane;
+            const int wrow = m * 2 * kBM + static_cast<int>(rank) * kBM + q * 32;  // first row of this warp
+            const int row = wrow + lane;
             const bool row_ok = row < p.M;
             const uint32_t tt = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                 static_cast<uint32_t>(acc * 256);
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+                if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
                 if (row_ok) {
                     const size_t o = static_cast<size_t>(n) * p.part_stride + row;
                     p.part_m[o] = mrun;
@@ -328,7 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
                 tc_fence_after();
-                const int out_row = m * kBM + q * 32;
 #pragma unroll 1
                 for (int c2 = 0; c2 < BN / 64; ++c2) {
                     const int col0 = v0 + c2 * 64;
@@ -362,20 +377,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_async_smem();
                     __syncwarp();
-                    if (lane == 0 && out_row < p.M) {
-                        tma_store_2d(&tmOut, buf, col0, out_row);
+                    if (lane == 0 && wrow < p.M) {
+                        tma_store_2d(&tmOut, buf, col0, wrow);
                         bulk_commit();
                     }
                     ++box;
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+                if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
             } else {
                 if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
                 tc_fence_after();
-                const int out_row = s * p.split_row_stride + m * kBM + q * 32;
-                const bool rows_ok = m * kBM + q * 32 < p.M;
+                const int out_row = s * p.split_row_stride + wrow;
+                const bool rows_ok = wrow < p.M;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     const int col0 = n * BN + c * 32;
@@ -401,63 +416,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+                if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
             }
         }
         if (EPI != EPI_LSE && lane == 0) bulk_wait_all();
         __syncwarp();
     }
 
+    // Neither CTA may leave while its peer can still touch its shared memory or TMEM.
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, 512);
+        tmem_dealloc_pair(tmem_base, 512);
     }
 }
 
 // ---------------------------------------------------------------- host dispatch
-int gemm_stages(int bn) { return bn == 128 ? TileCfg<128>::STAGES : TileCfg<256>::STAGES; }
-
-size_t gemm_smem_bytes(int bn, int epi) {
-    if (bn == 256) return epi == EPI_LSE ? smem_total<256, EPI_LSE>() : smem_total<256, EPI_F32>();
-    if (bn == 192) return epi == EPI_LSE ? smem_total<192, EPI_LSE>() : smem_total<192, EPI_F32>();
-    return epi == EPI_LSE ? smem_total<128, EPI_LSE>() : smem_total<128, EPI_F32>();
-}
-
 template <int BN, int A_MN, int B_MN, int EPI>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmOut,
-                              const GemmParams& p, int grid, cudaStream_t stream) {
-    constexpr size_t smem = smem_total<BN, EPI>();
+                              const GemmParams& p, int max_pairs, cudaStream_t stream) {
+    constexpr size_t smem = PairCfg<BN, B_MN, EPI>::SMEM;
     static_assert(smem <= 232448, "shared memory per CTA");
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, A_MN, B_MN, EPI>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static int pairs_resident = 0;
+    if (pairs_resident == 0) {
+        auto kern = gemm_kernel<BN, A_MN, B_MN, EPI>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured = true;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * max_pairs);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (e != cudaSuccess || clusters <= 0) {
+            cudaGetLastError();
+            clusters = max_pairs;
+        }
+        pairs_resident = clusters < max_pairs ? clusters : max_pairs;
     }
-    gemm_kernel<BN, A_MN, B_MN, EPI><<<grid, kThreads, smem, stream>>>(tmA, tmB, tmOut, p);
+    const long long units = static_cast<long long>(p.m_tiles) * p.n_tiles * p.splits;
+    const int pairs = static_cast<int>(units < pairs_resident ? units : pairs_resident);
+    gemm_kernel<BN, A_MN, B_MN, EPI><<<2 * pairs, kThreads, smem, stream>>>(tmA, tmB, tmOut, p);
     return cudaGetLastError();
+}
+
+size_t gemm_smem_bytes(int bn, int b_mn, int epi) {
+#define FKL_SMEM_CASE(BN_, B_, E_) \
+    if (bn == BN_ && b_mn == B_ && epi == E_) return PairCfg<BN_, B_, E_>::SMEM;
+    FKL_SMEM_CASE(256, 0, EPI_LSE) FKL_SMEM_CASE(256, 0, EPI_DZ)
+    FKL_SMEM_CASE(256, 0, EPI_F32) FKL_SMEM_CASE(256, 1, EPI_F32)
+    FKL_SMEM_CASE(192, 0, EPI_F32) FKL_SMEM_CASE(192, 1, EPI_F32)
+    FKL_SMEM_CASE(128, 0, EPI_F32) FKL_SMEM_CASE(128, 1, EPI_F32)
+#undef FKL_SMEM_CASE
+    return 0;
 }
 
 cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& tmA,
                         const CUtensorMap& tmB, const CUtensorMap& tmOut, const GemmParams& p,
-                        int grid, cudaStream_t stream) {
+                        int max_pairs, cudaStream_t stream) {
     if (epi == EPI_LSE) {
         if (bn == 256 && a_mn == 0 && b_mn == 0)
-            return launch_one<256, 0, 0, EPI_LSE>(tmA, tmB, tmOut, p, grid, stream);
+            return launch_one<256, 0, 0, EPI_LSE>(tmA, tmB, tmOut, p, max_pairs, stream);
         return cudaErrorInvalidValue;
     }
     if (epi == EPI_DZ) {
         if (bn == 256 && a_mn == 0 && b_mn == 0)
-            return launch_one<256, 0, 0, EPI_DZ>(tmA, tmB, tmOut, p, grid, stream);
+            return launch_one<256, 0, 0, EPI_DZ>(tmA, tmB, tmOut, p, max_pairs, stream);
         return cudaErrorInvalidValue;
     }
 #define FKL_F32_CASE(BN_, A_, B_)                                                       \
     if (bn == BN_ && a_mn == A_ && b_mn == B_)                                          \
-        return launch_one<BN_, A_, B_, EPI_F32>(tmA, tmB, tmOut, p, grid, stream);
+        return launch_one<BN_, A_, B_, EPI_F32>(tmA, tmB, tmOut, p, max_pairs, stream);
     FKL_F32_CASE(256, 0, 0) FKL_F32_CASE(256, 0, 1) FKL_F32_CASE(256, 1, 0) FKL_F32_CASE(256, 1, 1)
     FKL_F32_CASE(192, 0, 0) FKL_F32_CASE(192, 0, 1) FKL_F32_CASE(192, 1, 0) FKL_F32_CASE(192, 1, 1)
     FKL_F32_CASE(128, 0, 0) FKL_F32_CASE(128, 0, 1) FKL_F32_CASE(128, 1, 0) FKL_F32_CASE(128, 1, 1)
