@@ -11,8 +11,8 @@ torchrun (N > 1) every rank runs an independent replica of the same workload on
 its own GPU: the loss has no exchange step on one GPU per problem, so the job's
 value is the tokens of all ranks over the slowest rank's time.
 
-`--impl reference` times the fp64 CPU oracle instead, on a bounded row sample
-of the same workload per step (rank 0 only).
+`--impl reference` times the plain C++ fp64 CPU oracle instead, on a bounded row
+sample of the same workload per step (rank 0 only).
 """
 from __future__ import annotations
 
@@ -114,23 +114,21 @@ class ClockSampler:
 
 
 def threads_used():
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
-        if n:
-            return max(n)
-    except Exception:
-        pass
-    return os.cpu_count()
+    """Threads the C++ oracle runs on (it splits rows / vocabulary rows over them)."""
+    from oracle import cpp
+    return cpp.threads()
 
 
 def oracle_step_on_sample(x, rows, Wf):
-    """One oracle forward + backward over a row sample (the oracle as it stands)."""
-    import oracle
+    """One forward + backward of the plain C++ fp64 oracle (as it stands, all host
+    cores) over a row sample: the sampled rows form the batch, every row with the
+    full vocabulary and hidden size."""
+    from oracle import cpp
     from lm_head_kl_fkl_b300 import synth
+    orc = cpp.load()
     hs = synth.bf16_bits_to_f64(x["h"][rows])
-    f = oracle.forward(hs, Wf, x["idx"][rows], x["t"][rows], x["mask"][rows], x["T"])
-    g = oracle.backward(hs, Wf, x["idx"][rows], x["t"][rows], x["mask"][rows], x["T"])
+    f = orc.forward(hs, Wf, x["idx"][rows], x["t"][rows], x["mask"][rows], x["T"])
+    g = orc.backward(hs, Wf, x["idx"][rows], x["t"][rows], x["mask"][rows], x["T"])
     return f, g
 
 
@@ -139,18 +137,19 @@ def cpu_baseline(x, budget_s=12.0, max_rows=1024):
     from lm_head_kl_fkl_b300 import synth
     Wf = synth.bf16_bits_to_f64(x["W"])
     rng = np.random.default_rng(1)
-    rows = np.sort(rng.choice(x["N"], 8, replace=False))
+    probe = min(x["N"], max(8, threads_used()))  # one row per worker thread
+    rows = np.sort(rng.choice(x["N"], probe, replace=False))
     t0 = time.perf_counter()
     oracle_step_on_sample(x, rows, Wf)
     per_row = (time.perf_counter() - t0) / len(rows)
-    n = int(min(max_rows, max(8, budget_s / max(per_row, 1e-6))))
+    n = int(min(max_rows, x["N"], max(probe, budget_s / max(per_row, 1e-6))))
     rows = np.sort(rng.choice(x["N"], n, replace=False))
     t0 = time.perf_counter()
     oracle_step_on_sample(x, rows, Wf)
     dt = time.perf_counter() - t0
     return {"value": n / dt, "unit": "tokens/s", "cores": threads_used(), "kind": "oracle",
-            "sample": f"{n} seeded rows of the {x['name']} workload (full d and V), fp64 forward + "
-                      f"backward, {dt:.1f} s"}
+            "sample": f"{n} seeded rows of the {x['name']} workload (full d and V) as one batch, "
+                      f"plain C++ fp64 oracle forward + backward, {dt:.1f} s"}
 
 
 def workload(cfg, shape=None):
@@ -198,7 +197,8 @@ def run_reference(args):
             "data": "synthetic", "config": config_dict(c, args.chunk, 1),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads_used(),
                              "kind": "oracle",
-                             "sample": f"{n} seeded rows per step of the {c.name} workload, fp64"},
+                             "sample": f"{n} seeded rows per step of the {c.name} workload (full d and V) as "
+                                       f"one batch, plain C++ fp64 oracle forward + backward"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -365,7 +365,7 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--impl", choices=["fused", "reference"], default="fused")
-    ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--shape", type=lambda s: tuple(int(v) for v in s.split(",")), default=None,

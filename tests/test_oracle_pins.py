@@ -1,24 +1,54 @@
-"""The fp64 oracle against its pins, and planted mistakes against the pins.
+"""Both fp64 oracles (numpy and plain C++) against their pins, and planted
+mistakes against the pins.
 
-A planted mistake is a textual edit of a copy of the oracle's source, loaded as a
-separate module on the CPU; at least one pin must reject each mutant.
+A planted mistake is a textual edit of a copy of an oracle's source -- loaded as
+a separate module (numpy) or compiled into a separate library (C++) on the CPU;
+at least one pin must reject each mutant.  The two oracles are also compared with
+each other on the tiny workload (they share no code).
 """
 import importlib.util
 import os
 import types
 
+import numpy as np
 import pytest
 
 import oracle
+from oracle import cpp
+from lm_head_kl_fkl_b300 import synth
 from tests import oracle_pins as P
 
-ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                          "oracle", "fkl_oracle.py")
+ORACLE_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
+ORACLE_SRC = os.path.join(ORACLE_DIR, "fkl_oracle.py")
+
+
+@pytest.fixture(scope="module")
+def cpp_oracle():
+    return cpp.load()
 
 
 @pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
 def test_pin(pin):
     pin(oracle)
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin_cpp(pin, cpp_oracle):
+    pin(cpp_oracle)
+
+
+def test_numpy_and_cpp_oracles_agree_on_tiny_workload(cpp_oracle):
+    x = synth.config_inputs(0)
+    h, W = synth.bf16_bits_to_f64(x["h"]), synth.bf16_bits_to_f64(x["W"])
+    a = oracle.forward(h, W, x["idx"], x["t"], x["mask"], x["T"])
+    b = cpp_oracle.forward(h, W, x["idx"], x["t"], x["mask"], x["T"])
+    assert a["n_valid"] == b["n_valid"]
+    assert abs(a["loss"] - b["loss"]) <= 1e-12 * abs(a["loss"])
+    np.testing.assert_allclose(a["lse"], b["lse"], rtol=1e-13)
+    ga = oracle.backward(h, W, x["idx"], x["t"], x["mask"], x["T"])
+    gb = cpp_oracle.backward(h, W, x["idx"], x["t"], x["mask"], x["T"])
+    np.testing.assert_allclose(ga["dh"], gb["dh"], rtol=1e-9, atol=1e-15)
+    np.testing.assert_allclose(ga["dW"], gb["dW"], rtol=1e-9, atol=1e-15)
 
 
 def _mutant(old, new):
@@ -49,14 +79,48 @@ MUTATIONS = {
                               "return np.log(np.exp(a - m[:, None]).sum(axis=1))"),
 }
 
+# The same kinds of mistake, planted in the C++ oracle's source.
+CPP_MUTATIONS = {
+    "drop_T_squared": ("*loss = nv > 0 ? T * T * sum", "*loss = nv > 0 ? sum"),
+    "teacher_ignores_T": ("bool teacher_row(const double* t, int64_t K, double T, double* p) {",
+                          "bool teacher_row(const double* t, int64_t K, double T_, double* p) {\n"
+                          "    const double T = 1.0;\n    (void)T_;"),
+    "student_normaliser_truncated": ("lse[i] = lse_row(z.data(), V, T);\n            kl[i]",
+                                     "lse[i] = lse_row(z.data(), K, T);\n            kl[i]"),
+    "gradient_sign": ("dz[v] *= coef;", "dz[v] *= -coef;"),
+    "gradient_drops_teacher": ("for (int64_t k = 0; k < K; ++k) dz[idx[k]] -= p[k];", ""),
+    "index_off_by_one": ("const double logq = z[idx[k]] / T - lse;",
+                         "const double logq = z[idx[k] == 0 ? 1 : idx[k] - 1] / T - lse;"),
+    "mean_over_all_rows": ("T * T * sum / static_cast<double>(nv)", "T * T * sum / static_cast<double>(N)"),
+    "reverse_kl": ("kl += p[k] * (std::log(p[k]) - logq);", "kl += std::exp(logq) * (logq - std::log(p[k]));"),
+    "dW_rows_permuted": ("double* dwv = dW + v * d;", "double* dwv = dW + (V - 1 - v) * d;"),
+    "lse_missing_max_shift": ("return m + std::log(s);", "return std::log(s);"),
+    "dh_wrong_weight_row": ("dhi[j] += dzr[v] * W[v * d + j];", "dhi[j] += dzr[v] * W[((v + 1) % V) * d + j];"),
+}
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS))
-def test_planted_mistake_is_caught(name):
-    mod = _mutant(*MUTATIONS[name])
+
+def _rejected_by(mod):
     caught = []
     for pin in P.ALL_PINS:
         try:
             pin(mod)
         except Exception:  # AssertionError or a shape error both reject the mutant
             caught.append(pin.__name__)
-    assert caught, f"no pin rejects the planted mistake {name}"
+    return caught
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name):
+    assert _rejected_by(_mutant(*MUTATIONS[name])), f"no pin rejects the planted mistake {name}"
+
+
+@pytest.mark.parametrize("name", sorted(CPP_MUTATIONS))
+def test_planted_mistake_is_caught_cpp(name, tmp_path):
+    old, new = CPP_MUTATIONS[name]
+    with open(cpp.SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    mutant_src = tmp_path / "mutant.cpp"
+    mutant_src.write_text(src.replace(old, new))
+    lib = cpp.compile_library(str(mutant_src), str(tmp_path / "libmutant.so"))
+    assert _rejected_by(cpp.CppOracle(lib)), f"no pin rejects the planted mistake {name}"
