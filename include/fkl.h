@@ -81,6 +81,41 @@ fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const f
                        int chunk, float* loss, float* lse,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* Forward for callers that cannot allocate device memory: the same launch
+ * sequence and results as fkl_forward, with the workspace replaced by scratch
+ * that the library carries itself.  The pages have no counterpart to this entry
+ * point; it exists for callers that own no device allocator of their own (a
+ * plain C host program, or a plug-in running inside a runtime that has already
+ * reserved the GPU's memory for its own pool) and for step loops that must not
+ * call cudaMalloc/cudaFree, which can synchronise the device and can fail under
+ * memory pressure.
+ *
+ *  - Scratch: a fixed array of FKL_NOALLOC_SCRATCH_BYTES (64 MiB) in the
+ *    library's device image.  Every GPU that loads the library holds it until
+ *    the process exits.  This call allocates nothing: no cudaMalloc, cudaFree or
+ *    allocating library routine.
+ *  - Size limit: the forward needs 256 + 8*C*K + 5*C + 4*N + 12*C*ceil(V/256)
+ *    bytes (each term rounded up to 256) for chunk C (0 = 4096, capped at N
+ *    rounded up to 128); beyond FKL_NOALLOC_SCRATCH_BYTES the call returns
+ *    FKL_ERR_WORKSPACE before any launch, with the sizes in fkl_last_error.  At
+ *    V = 201088, K = 100 and C = 4096 that is about 42 MB + 4*N.
+ *  - Set-up: the first call on each device looks up the scratch's device
+ *    address (with that device current).  Make that first call before any
+ *    stream capture.
+ *  - Sharing: every call on a device uses the same scratch, which keeps the
+ *    previous call's contents (the call clears what must start at zero).  Calls
+ *    whose work overlaps on the GPU -- on different streams, or from different
+ *    host threads -- race on it: order them on one stream or with events.
+ *  - Device-side errors (a teacher id outside [0, V), a pipeline wait that
+ *    timed out) are copied, when the call's work finishes, into *status (one
+ *    int32 in device memory, caller-owned; NULL = not reported): FKL_OK or the
+ *    fkl_status code.
+ * Other arguments, preconditions and outputs are those of fkl_forward. */
+#define FKL_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+fkl_status fkl_forward_noalloc(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                               const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T,
+                               int chunk, float* loss, float* lse, int* status, void* stream);
+
 /* Backward: recomputes every logit tile and writes dh [N][d] (bf16, overwritten)
  * and dW [V][d] (fp32, overwritten).  `lse` is the forward's output for the same
  * inputs.  `grad_loss` points to one fp32 upstream gradient on the device

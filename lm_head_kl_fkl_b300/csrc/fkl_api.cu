@@ -164,6 +164,7 @@ struct Plan {
     int64_t N, V, Vs, n_chunks;
     int d, K, Cc, nt_v, bn_d, nt_d, splits;
     size_t o_sidx, o_sp, o_H, o_valid, o_rowloss, o_big, o_part_dh, total;
+    size_t fwd_total;  // bytes the forward alone touches (a prefix of the workspace)
 };
 
 int pick_bn(int d) {
@@ -245,6 +246,7 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
     const size_t part_dh = size_t(P.splits) * P.Cc * d * 4;
     P.o_part_dh = P.o_big + dz;
     P.total = P.o_big + std::max(part_fwd, dz + part_dh);
+    P.fwd_total = P.o_big + part_fwd;
     return true;
 }
 
@@ -304,46 +306,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 constexpr auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 
-}  // namespace
-}  // namespace fkl
-
-using namespace fkl;
-
-extern "C" {
-
-size_t fkl_workspace_size(int64_t N, int d, int64_t V, int K, int chunk) {
-    Plan P;
-    return make_plan(N, d, V, K, chunk, P) ? P.total : 0;
-}
-
-const char* fkl_status_string(fkl_status st) {
-    switch (st) {
-        case FKL_OK: return "ok";
-        case FKL_ERR_INVALID_ARG: return "invalid argument";
-        case FKL_ERR_WORKSPACE: return "workspace too small";
-        case FKL_ERR_INDEX: return "teacher index outside [0, V)";
-        case FKL_ERR_CUDA: return "CUDA error";
-        case FKL_ERR_UNSUPPORTED: return "unsupported device or size";
-        case FKL_ERR_TIMEOUT: return "device pipeline wait timed out";
-    }
-    return "unknown status";
-}
-
-const char* fkl_last_error(void) { return g_err; }
-
-fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
-                       const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T, int chunk,
-                       float* loss, float* lse, void* ws, size_t ws_bytes, void* stream) {
-    g_err[0] = 0;
-    if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
-        return fail(FKL_ERR_INVALID_ARG, "%s", e);
-    if (!loss || !lse) return fail(FKL_ERR_INVALID_ARG, "null loss or lse pointer");
-    Plan P;
-    make_plan(N, d, V, K, chunk, P);
-    if (ws_bytes < P.total)
-        return fail(FKL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, P.total);
-    if (fkl_status st = device_ready()) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// The forward's launch sequence on a workspace of at least P.fwd_total bytes
+// (sizes and pointers already checked).  Only the 256-byte header needs to start
+// at zero; it is cleared here.  Every other region is written before it is read.
+fkl_status forward_enqueue(const Plan& P, const void* h, const void* W, const int32_t* idx,
+                           const float* tlogit, const uint8_t* mask, float T, float* loss, float* lse,
+                           void* ws, cudaStream_t s) {
+    const int64_t N = P.N, V = P.V;
+    const int d = P.d, K = P.K;
     char* w = static_cast<char*>(ws);
     int* status = reinterpret_cast<int*>(w);
     int* n_valid = status + 1;
@@ -395,6 +365,105 @@ fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const f
                   launch_fwd_finalize(pm, pl, pg, P.Cc, P.nt_v, rows, H, valid, T, lse + row0, rowloss + row0, s));
     }
     FKL_SMALL(KK_LOSS_REDUCE, launch_loss_reduce(rowloss, N, n_valid, T, loss, s));
+    return FKL_OK;
+}
+}  // namespace
+}  // namespace fkl
+
+using namespace fkl;
+
+extern "C" {
+
+size_t fkl_workspace_size(int64_t N, int d, int64_t V, int K, int chunk) {
+    Plan P;
+    return make_plan(N, d, V, K, chunk, P) ? P.total : 0;
+}
+
+const char* fkl_status_string(fkl_status st) {
+    switch (st) {
+        case FKL_OK: return "ok";
+        case FKL_ERR_INVALID_ARG: return "invalid argument";
+        case FKL_ERR_WORKSPACE: return "workspace too small";
+        case FKL_ERR_INDEX: return "teacher index outside [0, V)";
+        case FKL_ERR_CUDA: return "CUDA error";
+        case FKL_ERR_UNSUPPORTED: return "unsupported device or size";
+        case FKL_ERR_TIMEOUT: return "device pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* fkl_last_error(void) { return g_err; }
+
+fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                       const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T, int chunk,
+                       float* loss, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    g_err[0] = 0;
+    if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
+        return fail(FKL_ERR_INVALID_ARG, "%s", e);
+    if (!loss || !lse) return fail(FKL_ERR_INVALID_ARG, "null loss or lse pointer");
+    Plan P;
+    make_plan(N, d, V, K, chunk, P);
+    if (ws_bytes < P.total)
+        return fail(FKL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, P.total);
+    if (fkl_status st = device_ready()) return st;
+    return forward_enqueue(P, h, W, idx, tlogit, mask, T, loss, lse, ws, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- forward without allocation
+// Scratch of fkl_forward_noalloc: a fixed array in the library's own device
+// image, present on every GPU that loads the library until the process exits.
+// Shared by every call; only its 256-byte header must start at zero, and the
+// forward clears it itself.
+static __device__ __align__(256) unsigned char g_fwd_scratch[FKL_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_fwd_scratch on the current device, looked up once per
+// device.  In host code `g_fwd_scratch` names a host-side stand-in, never the
+// device memory, so kernels are only ever given this looked-up address.
+static fkl_status noalloc_scratch(void** out) {
+    constexpr int kMaxDevices = 256;
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FKL_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(FKL_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fwd_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(FKL_ERR_CUDA, "cudaGetSymbolAddress of the forward scratch on device %d: %s", dev,
+                        cudaGetErrorString(e));
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return FKL_OK;
+}
+
+fkl_status fkl_forward_noalloc(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                               const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T, int chunk,
+                               float* loss, float* lse, int* status, void* stream) {
+    g_err[0] = 0;
+    const char* e = check_sizes(N, d, V, K, chunk);
+    if (!e && (!h || !W || !idx || !tlogit)) e = "null input pointer";
+    if (!e && (!(T > 0.f) || !std::isfinite(T))) e = "T must be positive and finite";
+    if (!e && (!aligned16(h) || !aligned16(W))) e = "h and W must be 16-byte aligned";
+    if (e) return fail(FKL_ERR_INVALID_ARG, "%s", e);
+    if (!loss || !lse) return fail(FKL_ERR_INVALID_ARG, "null loss or lse pointer");
+    Plan P;
+    make_plan(N, d, V, K, chunk, P);
+    if (P.fwd_total > FKL_NOALLOC_SCRATCH_BYTES)
+        return fail(FKL_ERR_WORKSPACE,
+                    "the forward needs %zu bytes of scratch for N=%lld, V=%lld, K=%d, chunk=%d; the built-in "
+                    "scratch holds %zu: pass a smaller chunk, or use fkl_forward with a caller workspace",
+                    P.fwd_total, static_cast<long long>(N), static_cast<long long>(V), K, P.Cc,
+                    static_cast<size_t>(FKL_NOALLOC_SCRATCH_BYTES));
+    if (fkl_status st = device_ready()) return st;
+    void* scratch = nullptr;
+    if (fkl_status st = noalloc_scratch(&scratch)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fkl_status st = forward_enqueue(P, h, W, idx, tlogit, mask, T, loss, lse, scratch, s)) return st;
+    if (status) FKL_CUDA_TRY(cudaMemcpyAsync(status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, s));
     return FKL_OK;
 }
 
