@@ -293,6 +293,37 @@ def run_fused(args):
                    **({"tflops": v[2] / (v[0] / 1e3) / 1e12} if v[2] > 0 else {})}
                for k, v in prof.items()}
 
+    # ---- the same step through fkl_forward_backward (one call, logits kept per chunk)
+    variants = None
+    if not args.no_variants:
+        def step_fb():
+            api.forward_backward(h, W, idx, t, mask, T, chunk=args.chunk, ws=ws, loss=loss, lse=lse, dh=dh, dW=dW)
+
+        for _ in range(args.warmup):
+            step_fb()
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        f0.record(stream)
+        for _ in range(args.steps):
+            step_fb()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        fms = f0.elapsed_time(f1)
+        if world > 1:
+            tt = torch.tensor([fms], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            fms = float(tt.item())
+        fstep = fms / args.steps
+        variants = {"forward_backward_one_call": {
+            "value": tokens / (fms / 1e3), "unit": "tokens/s", "ms_per_step": fstep,
+            "tflops_8NdV": flop_step / (fstep / 1e3) / 1e12,
+            "tensor_tflops_6NdV": 0.75 * flop_step / (fstep / 1e3) / 1e12,
+            "what": "fkl_forward_backward: each chunk's logits kept in fp16 between its loss and gradient "
+                    "passes instead of recomputed (6 N d V tensor FLOP)",
+            "device_status": api.get_status(ws)}}
+
     # ---- e2e: the public API with host buffers (pinned), copies inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -349,6 +380,7 @@ def run_fused(args):
                 "workspace_gb": ws.numel() / 1e9,
                 "resident_gb": base_mem / 1e9,
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "variants": variants,
                 "clocks": clk.summary(), "gpu_launches": launches, "device_status": status,
                 "kernel_digest": kernel_digest()}
         print(json.dumps(line), flush=True)
@@ -368,6 +400,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-variants", action="store_true", help="skip the one-call forward+backward timing")
     ap.add_argument("--shape", type=lambda s: tuple(int(v) for v in s.split(",")), default=None,
                     help="N,d,V,K: a smaller case of the chosen workload (profiling captures)")
     args = ap.parse_args()

@@ -127,6 +127,27 @@ fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const 
                         void* dh, float* dW,
                         void* ws, size_t ws_bytes, void* stream);
 
+/* Forward and backward in one call, for a training step that needs the loss
+ * gradient at once (the upstream gradient is known before the call; grad_loss
+ * NULL = 1.0).  Writes what fkl_forward followed by fkl_backward write: loss,
+ * lse [N], dh [N][d] (bf16) and dW [V][d] (fp32, overwritten).  Each chunk's
+ * logits are kept between the chunk's loss pass and its gradient pass, in the
+ * workspace's dz buffer, as fp16 y = z log2(e)/T minus the row's max over each
+ * 256-column vocabulary tile; dz is then formed from y in place.  The tensor
+ * cores therefore compute 6 N d V FLOP instead of 8 N d V, with the same
+ * workspace (fkl_workspace_size).  This is the forward-chunked alternative the
+ * pages weigh against recomputation ("Effektivnaya distillyatsiya znaniy",
+ * malakhovai.ru, the table of dense / forward-chunked / fused variants), here
+ * with per-chunk rather than per-sequence storage.  lse and loss equal
+ * fkl_forward's up to float rounding (the per-tile max / sum order differs); dz,
+ * hence dh and dW, differ from the recomputed ones by the fp16 rounding of y
+ * (relative 2^-11 of |y|, smallest where q is largest). */
+fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                                const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T,
+                                int chunk, const float* grad_loss, float* loss, float* lse,
+                                void* dh, float* dW,
+                                void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream` and returns the device status word of `ws` (FKL_OK if
  * no device-side error was recorded since the last call that used `ws`). */
 fkl_status fkl_get_status(const void* ws, void* stream);
@@ -155,7 +176,8 @@ int64_t fkl_launch_count(void);
  * C[M][N] (fp32, row-major) = sum_k A(m,k) B(n,k) on the same tcgen05/TMA
  * pipeline the loss kernels use.  a_mn = 0: A is [M][K] row-major (K-major);
  * a_mn = 1: A is stored [K][M] (M-major).  b_mn = 0: B is [N][K]; b_mn = 1: B
- * is stored [K][N].  bn selects the N tile (256, 192 or 128).  M, N, K >= 1 and
+ * is stored [K][N].  bn selects the N tile: 256, 192 or 128 (double-buffered
+ * accumulators), or 512 (two 256-wide sub-tiles sharing A, single-buffered).  M, N, K >= 1 and
  * multiples of 8.  `ws` (>= 256 bytes, device) receives the status word.  Used
  * to check the operand descriptors in isolation. */
 fkl_status fkl_selftest_gemm(const void* A, const void* B, float* C, int M, int N, int K,

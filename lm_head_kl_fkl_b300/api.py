@@ -120,6 +120,29 @@ def backward(h, W, idx, tlogit, mask, T: float, lse: torch.Tensor,
     return dh, dW
 
 
+def forward_backward(h, W, idx, tlogit, mask, T: float, grad_loss: Optional[torch.Tensor] = None,
+                     chunk: int = 0, ws: Optional[torch.Tensor] = None, loss: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, dh: Optional[torch.Tensor] = None,
+                     dW: Optional[torch.Tensor] = None):
+    """Loss and gradients in one call (logits kept per chunk, no recompute).
+
+    Returns (loss [1] fp32, lse [N] fp32, dh [N,d] bf16, dW [V,d] fp32)."""
+    N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
+    if grad_loss is not None:
+        _expect(grad_loss.reshape(-1), "grad_loss", torch.float32, 1, dev)
+    if ws is None:
+        ws = alloc_workspace(N, d, V, K, chunk, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
+    lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
+    dh = torch.empty((N, d), dtype=torch.bfloat16, device=dev) if dh is None else dh
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev) if dW is None else dW
+    st = _lib.lib().fkl_forward_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
+                                         float(T), int(chunk), _ptr(grad_loss), _ptr(loss), _ptr(lse),
+                                         _ptr(dh), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "fkl_forward_backward")
+    return loss, lse, dh, dW
+
+
 def get_status(ws: torch.Tensor) -> int:
     """Synchronises the current stream and returns the workspace's device status word."""
     return int(_lib.lib().fkl_get_status(_ptr(ws), _stream(ws.device)))

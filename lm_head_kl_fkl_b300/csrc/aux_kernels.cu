@@ -5,6 +5,7 @@
 #include <cmath>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fkl_internal.h"
 
@@ -184,6 +185,64 @@ __global__ void dh_reduce_kernel(const float4* __restrict__ part, int splits, si
         o.y = *reinterpret_cast<uint32_t*>(&hi);
         dh[i] = o;
     }
+}
+
+// dz of one chunk row from the logits its forward kept: y = z log2e/T - m_tile
+// (fp16, m_tile = part_m[tile][row], base 2), dz = coef (2^(y + m_tile - lse log2e)
+// - s) in bf16, written over y in place.  One block per row: the y at the teacher
+// ids are read first, then the whole row is rewritten, then the teacher entries
+// (each run of equal ids once, its p summed) are written with s subtracted.
+__global__ void dz_from_logits_kernel(uint16_t* __restrict__ yz, int64_t Vs, int64_t V,
+                                      const float* __restrict__ part_m, int stride,
+                                      const float* __restrict__ lse, const uint8_t* __restrict__ valid,
+                                      const int* __restrict__ n_valid, const float* __restrict__ grad, float T,
+                                      const int* __restrict__ sidx, const float* __restrict__ sp, int K) {
+    __shared__ float s_y[kMaxK];
+    constexpr float kLog2eF = 1.4426950408889634f;
+    const int r = blockIdx.x;
+    uint16_t* row = yz + static_cast<size_t>(r) * Vs;
+    const int* ids = sidx + static_cast<size_t>(r) * K;
+    const float* ps = sp + static_cast<size_t>(r) * K;
+    const float lse2 = lse[r] * kLog2eF;
+    const int nv = *n_valid;
+    const float coef = (valid[r] && nv > 0) ? T * (grad ? *grad : 1.f) / static_cast<float>(nv) : 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        const int v = ids[k];
+        s_y[k] = (v < V) ? __half2float(__ushort_as_half(row[v])) + part_m[static_cast<size_t>(v >> 8) * stride + r]
+                         : 0.f;
+    }
+    __syncthreads();
+    for (int64_t v = static_cast<int64_t>(threadIdx.x) * 8; v < V; v += static_cast<int64_t>(blockDim.x) * 8) {
+        const uint4 in = *reinterpret_cast<const uint4*>(row + v);
+        const float shift = part_m[static_cast<size_t>(v >> 8) * stride + r] - lse2;
+        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+            const float a = (v + 2 * j < V) ? coef * exp2f(y.x + shift) : 0.f;
+            const float b = (v + 2 * j + 1 < V) ? coef * exp2f(y.y + shift) : 0.f;
+            const __nv_bfloat162 ab = __floats2bfloat162_rn(a, b);
+            o[j] = *reinterpret_cast<const uint32_t*>(&ab);
+        }
+        *reinterpret_cast<uint4*>(row + v) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        const int v = ids[k];
+        if (v >= V || (k > 0 && ids[k - 1] == v)) continue;
+        float s = ps[k];
+        for (int j = k + 1; j < K && ids[j] == v; ++j) s += ps[j];
+        const __nv_bfloat16 d = __float2bfloat16_rn(coef * (exp2f(s_y[k] - lse2) - s));
+        row[v] = __bfloat16_as_ushort(d);
+    }
+}
+
+void launch_dz_from_logits(void* yz, int64_t Vs, int64_t V, const float* part_m, int part_stride,
+                           const float* lse, const uint8_t* valid, const int* n_valid, const float* grad,
+                           float T, const int* sidx, const float* sp, int K, int rows, cudaStream_t s) {
+    dz_from_logits_kernel<<<rows, 256, 0, s>>>(static_cast<uint16_t*>(yz), Vs, V, part_m, part_stride, lse, valid,
+                                               n_valid, grad, T, sidx, sp, K);
 }
 
 void launch_count_valid(const float* tlogit, const uint8_t* mask, int64_t N, int K, int* n_valid,

@@ -87,6 +87,7 @@ struct LaunchScope {
 const char* const kKindNames[KK_NUM] = {
     "count_valid", "teacher_prep", "fwd_gemm_lse", "fwd_finalize", "loss_reduce",
     "bwd_gemm_dz", "bwd_gemm_dh", "dh_reduce", "bwd_gemm_dw", "selftest_gemm",
+    "fb_gemm_lse_keep", "fb_dz_from_logits",
 };
 
 // ---------------------------------------------------------------- device facts
@@ -162,11 +163,13 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Plan {
     int64_t N, V, Vs, n_chunks;
-    int d, K, Cc, nt_v, bn_d, nt_d, splits;
+    int d, K, Cc, nt_v, bn_dh, nt_dh, bn_dw, nt_dw, splits;
     size_t o_sidx, o_sp, o_H, o_valid, o_rowloss, o_big, o_part_dh, total;
     size_t fwd_total;  // bytes the forward alone touches (a prefix of the workspace)
 };
 
+// Column tile of the dh and dW GEMMs (their N is d): the double-buffered width
+// that wastes the fewest padded columns.
 int pick_bn(int d) {
     const int cands[3] = {256, 192, 128};
     int best = 256;
@@ -179,6 +182,22 @@ int pick_bn(int d) {
         }
     }
     return best;
+}
+
+// From d = 384 on the operand traffic decides instead.  dh (k-loop over a V
+// split, tens of thousands deep) takes wide 512-column tiles, which move the
+// least operand data per FLOP.  dW (k-loop over one chunk's rows, a few thousand
+// deep, then a 256 x BN fp32 reduce-add) keeps 256-column double-buffered
+// tiles, so that its epilogue overlaps the next tile's MMAs.
+int pick_bn_dh(int d) { return d >= 384 ? 512 : pick_bn(d); }
+int pick_bn_dw(int d) { return d >= 384 ? 256 : pick_bn(d); }
+
+int bn_override(const char* name, int fallback) {
+    if (const char* e = getenv(name)) {  // tile-width override for tuning sweeps
+        const int v = atoi(e);
+        if (v == 512 || v == 256 || v == 192 || v == 128) return v;
+    }
+    return fallback;
 }
 
 // Split count of the dh GEMM over V: the smallest S whose units (pair tiles x S)
@@ -221,13 +240,11 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
     P.Cc = static_cast<int>(std::min<int64_t>(want, cdiv(N, kBM) * kBM));
     P.n_chunks = cdiv(N, P.Cc);
     P.nt_v = static_cast<int>(cdiv(V, kVocabTile));
-    P.bn_d = pick_bn(d);
-    if (const char* e = getenv("FKL_BN_D")) {  // tile-width override for tuning sweeps
-        const int v = atoi(e);
-        if (v == 256 || v == 192 || v == 128) P.bn_d = v;
-    }
-    P.nt_d = static_cast<int>(cdiv(d, P.bn_d));
-    P.splits = pick_splits(static_cast<int>(cdiv(P.Cc, kPairRows)), P.nt_d, cdiv(V, kBK));
+    P.bn_dh = bn_override("FKL_BN_DH", pick_bn_dh(d));
+    P.bn_dw = bn_override("FKL_BN_DW", pick_bn_dw(d));
+    P.nt_dh = static_cast<int>(cdiv(d, P.bn_dh));
+    P.nt_dw = static_cast<int>(cdiv(d, P.bn_dw));
+    P.splits = pick_splits(static_cast<int>(cdiv(P.Cc, kPairRows)), P.nt_dh, cdiv(V, kBK));
     P.Vs = cdiv(V, 8) * 8;
     size_t off = 256;  // header: status word, N_valid
     P.o_sidx = off;
@@ -245,7 +262,10 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
     const size_t dz = align256(size_t(P.Cc) * P.Vs * 2);
     const size_t part_dh = size_t(P.splits) * P.Cc * d * 4;
     P.o_part_dh = P.o_big + dz;
-    P.total = P.o_big + std::max(part_fwd, dz + part_dh);
+    // fkl_forward keeps its partials at o_big; fkl_backward puts dz there and
+    // the dh partials after it; fkl_forward_backward needs dz and the forward
+    // partials at once, so its partials share the dh partials' place.
+    P.total = P.o_big + dz + std::max(part_fwd, part_dh);
     P.fwd_total = P.o_big + part_fwd;
     return true;
 }
@@ -305,6 +325,44 @@ fkl_status run_gemm(int kind, int bn, int a_mn, int b_mn, int epi, const CUtenso
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 constexpr auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+constexpr auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+
+// dh and dW of chunk c from its dz ([rows][Vs] bf16 in the workspace):
+//   dh partials [split][rows][d] = dz[:, split's V range] W[split's V range, :],
+//   their fixed-order sum in bf16 into dh_chunk, and
+//   dW (+)= dz^T h_chunk (TMA store for chunk 0, reduce-add after; one owner per
+//   output tile, chunks in stream order).
+fkl_status grads_from_dz(const Plan& P, int64_t c, int rows, const CUtensorMap& tmDz_k, const CUtensorMap& tmDz_mn,
+                         const CUtensorMap& tmH_mn, const CUtensorMap& tmW_mn, const CUtensorMap& tmPart,
+                         const CUtensorMap& tmDW, float* part, void* dh_chunk, int* status, cudaStream_t s) {
+    const int d = P.d;
+    const double flop = 2.0 * rows * double(d) * double(P.V);
+    GemmParams q{};
+    q.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
+    q.n_tiles = P.nt_dh;
+    q.splits = P.splits;
+    q.kb_total = static_cast<int>(cdiv(P.V, kBK));
+    q.m_fastest = 0;  // pairs in flight cover every d tile of a few row tiles: dz is read once
+    q.M = rows;
+    q.Ncols = d;
+    q.status = status;
+    q.split_row_stride = P.Cc;
+    q.reduce = 0;
+    if (fkl_status st = run_gemm(KK_BWD_DH, P.bn_dh, 0, 1, EPI_F32, tmDz_k, tmW_mn, tmPart, q, flop, s)) return st;
+    FKL_SMALL(KK_DH_REDUCE, launch_dh_reduce(part, P.splits, size_t(P.Cc) * d, rows, d, dh_chunk, s));
+
+    GemmParams r{};
+    r.m_tiles = static_cast<int>(cdiv(P.V, kPairRows));
+    r.n_tiles = P.nt_dw;
+    r.splits = 1;
+    r.kb_total = static_cast<int>(cdiv(rows, kBK));
+    r.m_fastest = 0;
+    r.M = static_cast<int>(P.V);
+    r.Ncols = d;
+    r.status = status;
+    r.reduce = c > 0 ? 1 : 0;
+    return run_gemm(KK_BWD_DW, P.bn_dw, 1, 1, EPI_F32, tmDz_mn, tmH_mn, tmDW, r, flop, s);
+}
 
 // The forward's launch sequence on a workspace of at least P.fwd_total bytes
 // (sizes and pointers already checked).  Only the 256-byte header needs to start
@@ -536,37 +594,96 @@ fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const 
         p.T = T;
         if (fkl_status st = run_gemm(KK_BWD_DZ, 256, 0, 0, EPI_DZ, tmH_k, tmW_k, tmDz_st, p, flop, s)) return st;
 
-        // dh partials: [split][rows][d] = dz[:, split's V range] W[split's V range, :]
-        GemmParams q{};
-        q.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
-        q.n_tiles = P.nt_d;
-        q.splits = P.splits;
-        q.kb_total = static_cast<int>(cdiv(V, kBK));
-        q.m_fastest = 0;  // pairs in flight cover every d tile of a few row tiles: dz is read once
-        q.M = rows;
-        q.Ncols = d;
-        q.status = status;
-        q.split_row_stride = P.Cc;
-        q.reduce = 0;
-        if (fkl_status st = run_gemm(KK_BWD_DH, P.bn_d, 0, 1, EPI_F32, tmDz_k, tmW_mn, tmPart, q, flop, s))
-            return st;
-        FKL_SMALL(KK_DH_REDUCE, launch_dh_reduce(part, P.splits, size_t(P.Cc) * d, rows, d,
-                                                 static_cast<char*>(dh) + size_t(row0) * d * 2, s));
-
-        // dW (+)= dz^T h_chunk, one owner per output tile, chunks in order
-        GemmParams r{};
-        r.m_tiles = static_cast<int>(cdiv(V, kPairRows));
-        r.n_tiles = P.nt_d;
-        r.splits = 1;
-        r.kb_total = static_cast<int>(cdiv(rows, kBK));
-        r.m_fastest = 0;
-        r.M = static_cast<int>(V);
-        r.Ncols = d;
-        r.status = status;
-        r.reduce = c > 0 ? 1 : 0;
-        if (fkl_status st = run_gemm(KK_BWD_DW, P.bn_d, 1, 1, EPI_F32, tmDz_mn, tmH_mn, tmDW, r, flop, s))
+        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmH_mn, tmW_mn, tmPart, tmDW, part,
+                                          static_cast<char*>(dh) + size_t(row0) * d * 2, status, s))
             return st;
     }
+    return FKL_OK;
+}
+
+fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                                const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T, int chunk,
+                                const float* grad_loss, float* loss, float* lse, void* dh, float* dW, void* ws,
+                                size_t ws_bytes, void* stream) {
+    g_err[0] = 0;
+    if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
+        return fail(FKL_ERR_INVALID_ARG, "%s", e);
+    if (!loss || !lse || !dh || !dW) return fail(FKL_ERR_INVALID_ARG, "null loss, lse, dh or dW pointer");
+    if (!aligned16(dh) || !aligned16(dW)) return fail(FKL_ERR_INVALID_ARG, "dh and dW must be 16-byte aligned");
+    Plan P;
+    make_plan(N, d, V, K, chunk, P);
+    if (ws_bytes < P.total)
+        return fail(FKL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, P.total);
+    if (fkl_status st = device_ready()) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(ws);
+    int* status = reinterpret_cast<int*>(w);
+    int* n_valid = status + 1;
+    int* sidx = reinterpret_cast<int*>(w + P.o_sidx);
+    float* sp = reinterpret_cast<float*>(w + P.o_sp);
+    float* H = reinterpret_cast<float*>(w + P.o_H);
+    uint8_t* valid = reinterpret_cast<uint8_t*>(w + P.o_valid);
+    float* rowloss = reinterpret_cast<float*>(w + P.o_rowloss);
+    void* yz = w + P.o_big;  // kept logits (fp16), then dz (bf16) in place
+    float* part = reinterpret_cast<float*>(w + P.o_part_dh);
+    const size_t pstride = align256(size_t(P.nt_v) * P.Cc * 4);
+    float* pm = reinterpret_cast<float*>(w + P.o_part_dh);  // forward partials share the dh partials' place
+    float* pl = reinterpret_cast<float*>(w + P.o_part_dh + pstride);
+    float* pg = reinterpret_cast<float*>(w + P.o_part_dh + 2 * pstride);
+
+    FKL_CUDA_TRY(cudaMemsetAsync(w, 0, 256, s));
+    const int sms = device_info().sms;
+    FKL_SMALL(KK_COUNT_VALID, launch_count_valid(tlogit, mask, N, K, n_valid, sms * 4, s));
+
+    CUtensorMap tmW_k, tmW_mn, tmDW;
+    FKL_TMAP(tmW_k, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, kVocabTile / 2);
+    FKL_TMAP(tmW_mn, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 64);
+    FKL_TMAP(tmDW, F32, dW, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32);
+    for (int64_t c = 0; c < P.n_chunks; ++c) {
+        const int64_t row0 = c * P.Cc;
+        const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
+        FKL_SMALL(KK_TEACHER_PREP,
+                  launch_teacher_prep(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status, s));
+        const char* hc = static_cast<const char*>(h) + size_t(row0) * d * 2;
+        CUtensorMap tmH_k, tmH_mn, tmY_st, tmDz_k, tmDz_mn, tmPart;
+        FKL_TMAP(tmH_k, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 128);
+        FKL_TMAP(tmH_mn, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 64);
+        FKL_TMAP(tmY_st, F16, yz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 32);
+        FKL_TMAP(tmDz_k, BF16, yz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 128);
+        FKL_TMAP(tmDz_mn, BF16, yz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 64);
+        FKL_TMAP(tmPart, F32, part, uint64_t(d), uint64_t(P.splits) * P.Cc, uint64_t(d) * 4, 32, 32);
+
+        // logits of the chunk: lse / gather partials, and y = z log2e/T - tile max kept in fp16
+        GemmParams p{};
+        p.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
+        p.n_tiles = P.nt_v;
+        p.splits = 1;
+        p.kb_total = static_cast<int>(cdiv(d, kBK));
+        p.m_fastest = 1;
+        p.M = rows;
+        p.Ncols = static_cast<int>(V);
+        p.status = status;
+        p.scale2 = kLog2e / T;
+        p.sidx = sidx;
+        p.sp = sp;
+        p.K = K;
+        p.part_m = pm;
+        p.part_l = pl;
+        p.part_g = pg;
+        p.part_stride = P.Cc;
+        if (fkl_status st = run_gemm(KK_FB_GEMM_LSE_Y, 256, 0, 0, EPI_LSE_Y, tmH_k, tmW_k, tmY_st, p,
+                                     2.0 * rows * double(d) * double(V), s))
+            return st;
+        FKL_SMALL(KK_FWD_FINALIZE,
+                  launch_fwd_finalize(pm, pl, pg, P.Cc, P.nt_v, rows, H, valid, T, lse + row0, rowloss + row0, s));
+        // dz from the kept logits, in place (no second pass over the tensor cores)
+        FKL_SMALL(KK_FB_DZ, launch_dz_from_logits(yz, P.Vs, V, pm, P.Cc, lse + row0, valid, n_valid, grad_loss, T,
+                                                  sidx, sp, K, rows, s));
+        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmH_mn, tmW_mn, tmPart, tmDW, part,
+                                          static_cast<char*>(dh) + size_t(row0) * d * 2, status, s))
+            return st;
+    }
+    FKL_SMALL(KK_LOSS_REDUCE, launch_loss_reduce(rowloss, N, n_valid, T, loss, s));
     return FKL_OK;
 }
 
@@ -619,7 +736,8 @@ fkl_status fkl_selftest_gemm(const void* A, const void* B, float* C, int M, int 
     if (M < 1 || N < 1 || K < 1 || M % 8 || N % 8 || K % 8)
         return fail(FKL_ERR_INVALID_ARG, "M, N, K must be positive multiples of 8");
     if ((a_mn | b_mn) & ~1) return fail(FKL_ERR_INVALID_ARG, "a_mn and b_mn must be 0 or 1");
-    if (bn != 256 && bn != 192 && bn != 128) return fail(FKL_ERR_INVALID_ARG, "bn must be 256, 192 or 128");
+    if (bn != 512 && bn != 256 && bn != 192 && bn != 128)
+        return fail(FKL_ERR_INVALID_ARG, "bn must be 512, 256, 192 or 128");
     if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(ws))
         return fail(FKL_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     if (fkl_status st = device_ready()) return st;
@@ -628,7 +746,7 @@ fkl_status fkl_selftest_gemm(const void* A, const void* B, float* C, int M, int 
     CUtensorMap ta, tb, tc;
     if (a_mn == 0) FKL_TMAP(ta, BF16, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, 64, 128);
     else FKL_TMAP(ta, BF16, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, 64);
-    if (b_mn == 0) FKL_TMAP(tb, BF16, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, 64, uint32_t(bn / 2));
+    if (b_mn == 0) FKL_TMAP(tb, BF16, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, 64, uint32_t(std::min(bn, 256) / 2));
     else FKL_TMAP(tb, BF16, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, 64);
     FKL_TMAP(tc, F32, C, uint64_t(N), uint64_t(M), uint64_t(N) * 4, 32, 32);
     GemmParams p{};

@@ -30,10 +30,12 @@ enum KernelKind {
     KK_DH_REDUCE,
     KK_BWD_DW,       // tcgen05 GEMM dW (+)= dz^T h (TMA store / reduce-add)
     KK_SELFTEST,
+    KK_FB_GEMM_LSE_Y,  // tcgen05 GEMM z = h W^T, logsumexp / gather epilogue that also keeps the logits
+    KK_FB_DZ,          // dz from the kept logits (elementwise)
     KK_NUM
 };
 
-enum Epilogue { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2 };
+enum Epilogue { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_LSE_Y = 3 };
 
 // Parameters of one persistent GEMM launch.  The unit space is
 // m_tiles (of 256 rows) x n_tiles (of BN columns) x splits; unit u maps to (m, n, s) with s slowest and either
@@ -49,7 +51,7 @@ struct GemmParams {
     const int* sidx;   // [M][K] teacher ids sorted ascending (chunk-local rows)
     const float* sp;   // [M][K] teacher probabilities in the same order
     int K;
-    float* part_m;     // EPI_LSE: [n_tiles][part_stride] running max (base 2)
+    float* part_m;     // EPI_LSE(_Y): [n_tiles][part_stride] running (EPI_LSE_Y: tile) max, base 2
     float* part_l;     //          [n_tiles][part_stride] sum of 2^(y - max)
     float* part_g;     //          [n_tiles][part_stride] sum_k p_k z_{idx_k}
     int part_stride;
@@ -84,5 +86,8 @@ void launch_loss_reduce(const float* rowloss, int64_t N, const int* n_valid, flo
                         cudaStream_t s);
 void launch_dh_reduce(const float* part, int splits, size_t split_elems, int rows, int d, void* dh,
                       cudaStream_t s);
+void launch_dz_from_logits(void* yz, int64_t Vs, int64_t V, const float* part_m, int part_stride,
+                           const float* lse, const uint8_t* valid, const int* n_valid, const float* grad,
+                           float T, const int* sidx, const float* sp, int K, int rows, cudaStream_t s);
 
 }  // namespace fkl

@@ -10,12 +10,22 @@
 // Per SM this halves the B operand's L2->SMEM traffic and shared-memory reads
 // against a one-SM 128 x BN tile, and leaves room for a deeper TMA ring.
 //
+// Wide tiles (NSUB = 2, EPI_F32 only): a pair owns 256 x 512 outputs as two
+// N = 256 sub-tiles that share every A k-block, so each CTA loads 16 KB of A and
+// 32 KB of B per 64-deep k-block for twice the MMA work of a 256-wide tile: 25 %
+// less L2->SMEM traffic per FLOP.  The 512-column accumulator fills TMEM, so it
+// is single-buffered (the epilogue does not overlap the next tile's MMAs); this
+// pays where the k-loop is long against the epilogue (dh, dW).  On the last,
+// ragged column tile the second sub-tile's N shrinks to the valid columns
+// (rounded up to 64), and both CTAs load their halves of that narrower B.
+//
 // Roles, in each CTA of the pair (192 threads, one CTA per SM):
 //   warp 0      one lane issues the CTA's TMA loads of A and B k-blocks into a
 //               STAGES-deep ring (128-byte swizzle); both CTAs' copies complete
 //               on the even CTA's `full` barrier, which the even CTA arms with
 //               the byte count of the pair;
-//   warp 1      allocates 512 TMEM columns (two accumulators) for the pair; in
+//   warp 1      allocates 512 TMEM columns (two 256-column accumulators, or one
+//               512-column accumulator for wide tiles) for the pair; in
 //               the even CTA one lane issues the MMAs, commits `empty` (stage
 //               reusable) and `tfull` (accumulator complete) to both CTAs;
 //   warps 2-5   the epilogue: each warp drains its 32 TMEM lanes (= 32 output
@@ -29,6 +39,12 @@
 //   EPI_DZ   the same logits recomputed: dz = coef * (2^(z log2e/T - lse log2e) - s)
 //            in bf16, staged per warp in swizzled shared memory and TMA-stored.
 //   EPI_F32  plain fp32 tile, TMA-stored or TMA reduce-added (dh partials, dW).
+//   EPI_LSE_Y  EPI_LSE for a forward whose backward follows at once: a first
+//            pass over the tile finds each row's tile max (and gathers the
+//            teacher logits), a second sums 2^(y) and keeps y = z log2e / T - max
+//            in fp16 (staged like EPI_DZ, TMA-stored), so that dz can later be
+//            formed from y without recomputing the tile.  Relative to the tile
+//            max, y is exact to 2^-11 of |y| where q is largest.
 //
 // Operand majorness (template): K-major tiles arrive as one TMA box {64, rows};
 // MN-major tiles as boxes {64 (MN), 64 (K)} side by side, 8 KB apart.
@@ -39,14 +55,17 @@
 
 namespace fkl {
 
-template <int BN, int B_MN, int EPI>
+template <int BN, int NSUB, int B_MN, int EPI>
 struct PairCfg {
-    static constexpr int BNH = BN / 2;                     // B columns held by one CTA
+    static constexpr int BNH = BN / 2;                     // B columns of one sub-tile held by one CTA
+    static constexpr int TW = BN * NSUB;                   // output columns of a pair tile
+    static constexpr int NBUF = NSUB == 1 ? 2 : 1;         // TMEM accumulator buffers
     static constexpr uint32_t A_BYTES = kBM * kBK * 2;     // 128 rows x 64 k, bf16
     static constexpr int B_BOXES = B_MN ? (BNH + 63) / 64 : 1;
-    static constexpr uint32_t B_BYTES = B_MN ? B_BOXES * 8192u : static_cast<uint32_t>(BNH) * 128u;
+    static constexpr uint32_t B_SUB_BYTES = B_MN ? B_BOXES * 8192u : static_cast<uint32_t>(BNH) * 128u;
+    static constexpr uint32_t B_BYTES = NSUB * B_SUB_BYTES;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t STAGING_BYTES = EPI == EPI_LSE ? 0u : 4u * 2u * 4096u;
+    static constexpr uint32_t STAGING_BYTES = EPI == EPI_LSE ? 0u : 4u * 2u * 4096u;  // 2 x 4 KB per epilogue warp
     static constexpr uint32_t RING_BUDGET = 196608u + (EPI == EPI_LSE ? 32768u : 0u);
     static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) > 8 ? 8 : (RING_BUDGET / STAGE_BYTES);
     static constexpr uint32_t BAR_BYTES = 256;
@@ -115,16 +134,29 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <int BN, int A_MN, int B_MN, int EPI>
+// Width of sub-tile j of column tile n: BN, except the second sub-tile of a
+// ragged last wide tile, which covers the valid columns rounded up to 64 (0 if
+// none are left).
+template <int BN, int NSUB>
+__device__ __forceinline__ int sub_width(const GemmParams& p, int n, int j) {
+    if (NSUB == 1 || j == 0) return BN;
+    const int rest = p.Ncols - n * BN * NSUB - j * BN;
+    if (rest >= BN) return BN;
+    return rest <= 0 ? 0 : (rest + 63) & ~63;
+}
+
+template <int BN, int NSUB, int A_MN, int B_MN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-    using C = PairCfg<BN, B_MN, EPI>;
+    using C = PairCfg<BN, NSUB, B_MN, EPI>;
     constexpr int STAGES = C::STAGES;
-    constexpr int BNH = C::BNH;
+    constexpr int TW = C::TW;
+    constexpr int NBUF = C::NBUF;
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
-    static_assert(EPI != EPI_DZ || BN % 64 == 0, "dz boxes are 64 columns");
-    static_assert(B_MN || BNH <= 256, "K-major B box height");
+    static_assert(NSUB == 1 || (NSUB == 2 && BN == 256 && EPI == EPI_F32), "wide tiles: 2 x 256, fp32 epilogue");
+    static_assert((EPI != EPI_DZ && EPI != EPI_LSE_Y) || BN % 64 == 0, "dz / logit boxes are 64 columns");
+    static_assert(B_MN || BN / 2 <= 256, "K-major B box height");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -182,7 +214,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 decode_unit(u, p, m, n, s);
                 const int kb0 = kb_begin(p, s), kb1 = kb_begin(p, s + 1);
                 const int arow = m * 2 * kBM + static_cast<int>(rank) * kBM;
-                const int bcol = n * BN + static_cast<int>(rank) * BNH;
+                int bcol[NSUB];  // first B column of this CTA's half of each sub-tile
+#pragma unroll
+                for (int j = 0; j < NSUB; ++j)
+                    bcol[j] = n * TW + j * BN + static_cast<int>(rank) * (sub_width<BN, NSUB>(p, n, j) / 2);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, s_abort, p.status)) {
                         ok = false;
@@ -197,12 +232,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tma_load_2d_pair(sa, &tmA, fb, arow, kb * kBK);
                         tma_load_2d_pair(sa + 8192u, &tmA, fb, arow + 64, kb * kBK);
                     }
-                    if (B_MN == 0) {
-                        tma_load_2d_pair(sb, &tmB, fb, kb * kBK, bcol);
-                    } else {
 #pragma unroll
-                        for (int j = 0; j < C::B_BOXES; ++j)
-                            tma_load_2d_pair(sb + 8192u * j, &tmB, fb, bcol + 64 * j, kb * kBK);
+                    for (int j = 0; j < NSUB; ++j) {
+                        const uint32_t sbj = sb + j * C::B_SUB_BYTES;
+                        if (B_MN == 0) {
+                            tma_load_2d_pair(sbj, &tmB, fb, kb * kBK, bcol[j]);
+                        } else {
+#pragma unroll
+                            for (int b = 0; b < C::B_BOXES; ++b)
+                                tma_load_2d_pair(sbj + 8192u * b, &tmB, fb, bcol[j] + 64 * b, kb * kBK);
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -221,7 +260,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && leader) {
-            constexpr uint32_t IDESC = umma_idesc_bf16(2 * kBM, BN, A_MN, B_MN);
             int stage = 0, tc = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -229,8 +267,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 int m, n, s;
                 decode_unit(u, p, m, n, s);
                 const int kb0 = kb_begin(p, s), kb1 = kb_begin(p, s + 1);
-                const int acc = tc & 1;
-                const uint32_t aph = (tc >> 1) & 1;
+                const int acc = tc % NBUF;
+                const uint32_t aph = (tc / NBUF) & 1;
+                uint32_t idesc[NSUB];
+                int width[NSUB];
+#pragma unroll
+                for (int j = 0; j < NSUB; ++j) {
+                    width[j] = sub_width<BN, NSUB>(p, n, j);
+                    idesc[j] = umma_idesc_bf16(2 * kBM, width[j] > 0 ? width[j] : BN, A_MN, B_MN);
+                }
                 if (!mbar_wait(tempty0 + 8u * acc, aph ^ 1u, s_abort, p.status)) {
                     ok = false;
                     break;
@@ -248,9 +293,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * kk, 8192u, 1024u)
                                                  : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
-                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048u * kk, 8192u, 1024u)
-                                                 : smem_desc_sw128(sb + 32u * kk, 16u, 1024u);
-                        umma_bf16_pair(dt, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int j = 0; j < NSUB; ++j) {
+                            if (width[j] == 0) continue;
+                            const uint32_t sbj = sb + j * C::B_SUB_BYTES;
+                            const uint64_t bd = B_MN ? smem_desc_sw128(sbj + 2048u * kk, 8192u, 1024u)
+                                                     : smem_desc_sw128(sbj + 32u * kk, 16u, 1024u);
+                            umma_bf16_pair(dt + static_cast<uint32_t>(j * BN), ad, bd, idesc[j],
+                                           (kb > kb0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit_pair(empty0 + 8u * stage);
                     if (++stage == STAGES) {
@@ -275,8 +326,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int u = pair; u < units; u += npairs, ++tc) {
             int m, n, s;
             decode_unit(u, p, m, n, s);
-            const int acc = tc & 1;
-            const uint32_t aph = (tc >> 1) & 1;
+            const int acc = tc % NBUF;
+            const uint32_t aph = (tc / NBUF) & 1;
             const int wrow = m * 2 * kBM + static_cast<int>(rank) * kBM + q * 32;  // first row of this warp
             const int row = wrow + lane;
             const bool row_ok = row < p.M;
@@ -329,6 +380,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const size_t o = static_cast<size_t>(n) * p.part_stride + row;
                     p.part_m[o] = mrun;
                     p.part_l[o] = lrun;
+                    p.part_g[o] = g;
+                }
+            } else if constexpr (EPI == EPI_LSE_Y) {
+                const int v0 = n * BN;
+                TeacherCursor cur;
+                cur.seek(p.sidx, p.sp, row, row_ok, p.K, v0);
+                if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
+                tc_fence_after();
+                // pass 1: the row's max over this tile and the teacher gather
+                float mt = -INFINITY, g = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int col0 = v0 + c * 32;
+                    if (col0 >= p.Ncols) break;
+                    float z[32];
+                    __syncwarp();
+                    tmem_ld32(tt + c * 32, z);
+                    while (cur.next_id < col0 + 32) {
+                        g += cur.next_p * select32(z, cur.next_id - col0);
+                        cur.advance();
+                    }
+                    const int nv = p.Ncols - col0;
+                    float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        cm0 = fmaxf(cm0, (j < nv) ? z[j] : -INFINITY);
+                        cm1 = fmaxf(cm1, (j + 1 < nv) ? z[j + 1] : -INFINITY);
+                    }
+                    mt = fmaxf(mt, fmaxf(cm0, cm1));
+                }
+                mt *= p.scale2;  // scale2 > 0: the max of the scaled logits
+                // pass 2: sum of 2^(y) and y = z scale2 - mt kept in fp16, 64 columns per TMA box
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll 1
+                for (int c2 = 0; c2 < BN / 64; ++c2) {
+                    const int col0 = v0 + c2 * 64;
+                    if (col0 >= p.Ncols) break;
+                    const uint32_t buf = staging0 + static_cast<uint32_t>(q * 2 + (box & 1)) * 4096u;
+                    if (lane == 0) bulk_wait_read_le1();
+                    __syncwarp();
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int cc = col0 + hh * 32;
+                        float z[32];
+                        __syncwarp();
+                        tmem_ld32(tt + c2 * 64 + hh * 32, z);
+                        const int nv = p.Ncols - cc;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            z[j] = z[j] * p.scale2 - mt;
+                            z[j + 1] = z[j + 1] * p.scale2 - mt;
+                            l0 += (j < nv) ? ex2_approx(z[j]) : 0.f;
+                            l1 += (j + 1 < nv) ? ex2_approx(z[j + 1]) : 0.f;
+                        }
+                        uint32_t w[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) w[j] = pack_f16x2(z[2 * j], z[2 * j + 1]);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            st_shared_v4(buf + lane * 128u + ((static_cast<uint32_t>(hh * 4 + k) ^ (lane & 7u)) << 4),
+                                         w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && wrow < p.M) {
+                        tma_store_2d(&tmOut, buf, col0, wrow);
+                        bulk_commit();
+                    }
+                    ++box;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
+                if (row_ok) {
+                    const size_t o = static_cast<size_t>(n) * p.part_stride + row;
+                    p.part_m[o] = mt;
+                    p.part_l[o] = l0 + l1;
                     p.part_g[o] = g;
                 }
             } else if constexpr (EPI == EPI_DZ) {
@@ -392,8 +520,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int out_row = s * p.split_row_stride + wrow;
                 const bool rows_ok = wrow < p.M;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    const int col0 = n * BN + c * 32;
+                for (int c = 0; c < TW / 32; ++c) {
+                    const int col0 = n * TW + c * 32;
                     if (col0 >= p.Ncols) break;
                     const uint32_t buf = staging0 + static_cast<uint32_t>(q * 2 + (box & 1)) * 4096u;
                     if (lane == 0) bulk_wait_read_le1();
@@ -433,14 +561,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host dispatch
-template <int BN, int A_MN, int B_MN, int EPI>
+template <int BN, int NSUB, int A_MN, int B_MN, int EPI>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmOut,
                               const GemmParams& p, int max_pairs, cudaStream_t stream) {
-    constexpr size_t smem = PairCfg<BN, B_MN, EPI>::SMEM;
+    constexpr size_t smem = PairCfg<BN, NSUB, B_MN, EPI>::SMEM;
     static_assert(smem <= 232448, "shared memory per CTA");
     static int pairs_resident = 0;
     if (pairs_resident == 0) {
-        auto kern = gemm_kernel<BN, A_MN, B_MN, EPI>;
+        auto kern = gemm_kernel<BN, NSUB, A_MN, B_MN, EPI>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
@@ -458,17 +586,18 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, co
     }
     const long long units = static_cast<long long>(p.m_tiles) * p.n_tiles * p.splits;
     const int pairs = static_cast<int>(units < pairs_resident ? units : pairs_resident);
-    gemm_kernel<BN, A_MN, B_MN, EPI><<<2 * pairs, kThreads, smem, stream>>>(tmA, tmB, tmOut, p);
+    gemm_kernel<BN, NSUB, A_MN, B_MN, EPI><<<2 * pairs, kThreads, smem, stream>>>(tmA, tmB, tmOut, p);
     return cudaGetLastError();
 }
 
 size_t gemm_smem_bytes(int bn, int b_mn, int epi) {
-#define FKL_SMEM_CASE(BN_, B_, E_) \
-    if (bn == BN_ && b_mn == B_ && epi == E_) return PairCfg<BN_, B_, E_>::SMEM;
-    FKL_SMEM_CASE(256, 0, EPI_LSE) FKL_SMEM_CASE(256, 0, EPI_DZ)
-    FKL_SMEM_CASE(256, 0, EPI_F32) FKL_SMEM_CASE(256, 1, EPI_F32)
-    FKL_SMEM_CASE(192, 0, EPI_F32) FKL_SMEM_CASE(192, 1, EPI_F32)
-    FKL_SMEM_CASE(128, 0, EPI_F32) FKL_SMEM_CASE(128, 1, EPI_F32)
+#define FKL_SMEM_CASE(BN_, NS_, B_, E_) \
+    if (bn == BN_ * NS_ && b_mn == B_ && epi == E_) return PairCfg<BN_, NS_, B_, E_>::SMEM;
+    FKL_SMEM_CASE(256, 1, 0, EPI_LSE) FKL_SMEM_CASE(256, 1, 0, EPI_DZ) FKL_SMEM_CASE(256, 1, 0, EPI_LSE_Y)
+    FKL_SMEM_CASE(256, 2, 0, EPI_F32) FKL_SMEM_CASE(256, 2, 1, EPI_F32)
+    FKL_SMEM_CASE(256, 1, 0, EPI_F32) FKL_SMEM_CASE(256, 1, 1, EPI_F32)
+    FKL_SMEM_CASE(192, 1, 0, EPI_F32) FKL_SMEM_CASE(192, 1, 1, EPI_F32)
+    FKL_SMEM_CASE(128, 1, 0, EPI_F32) FKL_SMEM_CASE(128, 1, 1, EPI_F32)
 #undef FKL_SMEM_CASE
     return 0;
 }
@@ -478,20 +607,26 @@ cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& 
                         int max_pairs, cudaStream_t stream) {
     if (epi == EPI_LSE) {
         if (bn == 256 && a_mn == 0 && b_mn == 0)
-            return launch_one<256, 0, 0, EPI_LSE>(tmA, tmB, tmOut, p, max_pairs, stream);
+            return launch_one<256, 1, 0, 0, EPI_LSE>(tmA, tmB, tmOut, p, max_pairs, stream);
         return cudaErrorInvalidValue;
     }
     if (epi == EPI_DZ) {
         if (bn == 256 && a_mn == 0 && b_mn == 0)
-            return launch_one<256, 0, 0, EPI_DZ>(tmA, tmB, tmOut, p, max_pairs, stream);
+            return launch_one<256, 1, 0, 0, EPI_DZ>(tmA, tmB, tmOut, p, max_pairs, stream);
         return cudaErrorInvalidValue;
     }
-#define FKL_F32_CASE(BN_, A_, B_)                                                       \
-    if (bn == BN_ && a_mn == A_ && b_mn == B_)                                          \
-        return launch_one<BN_, A_, B_, EPI_F32>(tmA, tmB, tmOut, p, max_pairs, stream);
-    FKL_F32_CASE(256, 0, 0) FKL_F32_CASE(256, 0, 1) FKL_F32_CASE(256, 1, 0) FKL_F32_CASE(256, 1, 1)
-    FKL_F32_CASE(192, 0, 0) FKL_F32_CASE(192, 0, 1) FKL_F32_CASE(192, 1, 0) FKL_F32_CASE(192, 1, 1)
-    FKL_F32_CASE(128, 0, 0) FKL_F32_CASE(128, 0, 1) FKL_F32_CASE(128, 1, 0) FKL_F32_CASE(128, 1, 1)
+    if (epi == EPI_LSE_Y) {
+        if (bn == 256 && a_mn == 0 && b_mn == 0)
+            return launch_one<256, 1, 0, 0, EPI_LSE_Y>(tmA, tmB, tmOut, p, max_pairs, stream);
+        return cudaErrorInvalidValue;
+    }
+#define FKL_F32_CASE(BN_, NS_, A_, B_)                                                      \
+    if (bn == BN_ * NS_ && a_mn == A_ && b_mn == B_)                                        \
+        return launch_one<BN_, NS_, A_, B_, EPI_F32>(tmA, tmB, tmOut, p, max_pairs, stream);
+    FKL_F32_CASE(256, 2, 0, 0) FKL_F32_CASE(256, 2, 0, 1) FKL_F32_CASE(256, 2, 1, 0) FKL_F32_CASE(256, 2, 1, 1)
+    FKL_F32_CASE(256, 1, 0, 0) FKL_F32_CASE(256, 1, 0, 1) FKL_F32_CASE(256, 1, 1, 0) FKL_F32_CASE(256, 1, 1, 1)
+    FKL_F32_CASE(192, 1, 0, 0) FKL_F32_CASE(192, 1, 0, 1) FKL_F32_CASE(192, 1, 1, 0) FKL_F32_CASE(192, 1, 1, 1)
+    FKL_F32_CASE(128, 1, 0, 0) FKL_F32_CASE(128, 1, 0, 1) FKL_F32_CASE(128, 1, 1, 0) FKL_F32_CASE(128, 1, 1, 1)
 #undef FKL_F32_CASE
     return cudaErrorInvalidValue;
 }

@@ -24,13 +24,13 @@ def _case(M, N, K, a_mn, b_mn, bn, seed=0):
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
-@pytest.mark.parametrize("bn", [256, 192, 128])
+@pytest.mark.parametrize("bn", [512, 256, 192, 128])
 def test_single_tile_exact_k(a_mn, b_mn, bn):
     _case(128, bn, 64, a_mn, b_mn, bn)
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
-@pytest.mark.parametrize("bn", [256, 192, 128])
+@pytest.mark.parametrize("bn", [512, 256, 192, 128])
 def test_ragged_multi_tile(a_mn, b_mn, bn):
     # tails in M, N and K; several k-blocks and tiles per CTA
     _case(392, 584, 456, a_mn, b_mn, bn, seed=1)
@@ -40,3 +40,13 @@ def test_ragged_multi_tile(a_mn, b_mn, bn):
 def test_many_tiles_persistent(a_mn, b_mn):
     # more tiles than SMs: exercises the double-buffered accumulator and ring wrap-around
     _case(2048, 2304, 2880, a_mn, b_mn, 192 if b_mn else 256, seed=2)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 1), (1, 1), (0, 0)])
+@pytest.mark.parametrize("N", [2880, 2816, 2624, 2936, 2968, 2504, 2560])
+def test_wide_tiles_ragged_last_sub_tile(a_mn, b_mn, N):
+    # 512-wide tiles.  Columns left for the last tile's second sub-tile, and the
+    # sub-tile width that follows: 2880: 64 -> 64; 2816: 0 -> skipped; 2624: the
+    # first sub-tile is itself ragged; 2936: 120 -> 128; 2968: 152 -> 192;
+    # 2504: 200 -> 256; 2560: no ragged tile.
+    _case(1000, N, 1216, a_mn, b_mn, 512, seed=3)

@@ -133,3 +133,33 @@ def test_autograd_loss_matches_oracle():
     assert rel_l2(h.grad.double().cpu().numpy(), g["dh"]) <= TOL_GRAD_REL_L2
     assert rel_l2(W.grad.double().cpu().numpy(), g["dW"]) <= TOL_GRAD_REL_L2
     assert torch.isfinite(h.grad).all()
+
+
+def test_row_shards_combine_to_full_batch():
+    """The data-parallel reading of the loss, run shard after shard on one GPU.
+
+    Rows split into R shards; shard r runs on its own with the upstream gradient
+    g_r = N_valid_r / N_valid, so that its dz carries the global 1/N_valid.  Then
+    loss = sum_r loss_r N_valid_r / N_valid, dh is the shards' dh stacked and
+    dW = sum_r dW_r -- the only exchange a row-sharded job needs (the global
+    N_valid before the step, one sum of loss and dW after it)."""
+    x = synth.make_inputs(1100, 192, 3000, 24, 1.0, 0.05, "uniform", seed=90)
+    full = run_fused(to_device(x), chunk=256)
+    valid = oracle.row_valid(x["mask"], x["t"], x["T"])
+    n_valid = int(valid.sum())
+    bounds = [0, 300, 700, 1100]
+    loss, dW, dh, lse = 0.0, 0.0, [], []
+    for r0, r1 in zip(bounds[:-1], bounds[1:]):
+        xs = dict(x, h=x["h"][r0:r1], idx=x["idx"][r0:r1], t=x["t"][r0:r1], mask=x["mask"][r0:r1])
+        nv_r = int(valid[r0:r1].sum())
+        out = run_fused(to_device(xs), chunk=256, grad=nv_r / n_valid)
+        loss += out["loss"] * nv_r / n_valid
+        dW = dW + out["dW"]
+        dh.append(out["dh"])
+        lse.append(out["lse"])
+    # per-row work does not depend on which rows share a launch
+    assert np.array_equal(np.concatenate(lse), full["lse"])
+    assert abs(loss - full["loss"]) <= 1e-5 * abs(full["loss"])
+    assert rel_l2(np.concatenate(dh), full["dh"]) <= 1e-3
+    assert rel_l2(dW, full["dW"]) <= 1e-4
+    _check(x, dict(loss=loss, lse=np.concatenate(lse), dh=np.concatenate(dh), dW=dW))
