@@ -34,9 +34,11 @@ METRIC = "fused top-K KL fwd+bwd tokens/s at V=201088; % of bf16 tensor peak; pe
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the
-# kernel source digest they were taken on (see profiles/); stale digests give null.
-TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the dominant kernel at the default
+# gpt-oss-20b-like workload, from an ncu capture of a smaller case scaled by the
+# units processed, keyed by the kernel source digest they were taken on (see
+# profiles/dw_gemm_traffic.md); a stale digest gives null.
+TRAFFIC = {("bwd_gemm_dw", "98a722b46a4c"): 6.03e9}
 
 
 def load_peaks():
@@ -286,7 +288,9 @@ def run_fused(args):
         peak = peaks["bf16_tflops_sustained"]
         dig = kernel_digest()
         roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                    "unit": "TFLOP/s", "frac": achieved / peak, "traffic": TRAFFIC.get((dom, dig)),
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "traffic": TRAFFIC.get((dom, dig)) if args.config == 3 and args.shape is None and not args.chunk
+                    else None,
                     "peak_kind": f"bf16 dense, sustained, {peaks_kind}",
                     "flop_per_launch": fl / n_l, "launch_ms": tot_ms / n_l, "launches": n_l}
     kernels = {k: {"ms_total": v[0], "launches": v[1], "share": v[0] / max(1e-9, sum(p[0] for p in prof.values())),
