@@ -328,6 +328,28 @@ def run_fused(args):
                     "passes instead of recomputed (6 N d V tensor FLOP)",
             "device_status": api.get_status(ws)}}
 
+    # ---- the teacher top-K cache producer on the same shapes (h, W standing in for the teacher's)
+    topk = None
+    if not args.no_variants:
+        tk_ws = torch.empty(api.topk_workspace_size(N, d, V, K), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            api.teacher_topk(h, W, K, ws=tk_ws)
+        torch.cuda.synchronize()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        for _ in range(args.steps):
+            api.teacher_topk(h, W, K, ws=tk_ws)
+        k1.record(stream)
+        torch.cuda.synchronize()
+        kstep = k0.elapsed_time(k1) / args.steps
+        topk = {"value": N / (kstep / 1e3), "unit": "tokens/s", "ms_per_step": kstep,
+                "tflops_4NdV": 4.0 * N * d * V / (kstep / 1e3) / 1e12, "K": K,
+                "workspace_gb": tk_ws.numel() / 1e9,
+                "what": "fkl_teacher_topk: two tensor-core passes over z = h W^T (per-tile max, then the "
+                        "logits above the K-th largest tile max), top-K selection per row",
+                "device_status": api.get_status(tk_ws)}
+        del tk_ws
+
     # ---- e2e: the public API with host buffers (pinned), copies inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -384,7 +406,7 @@ def run_fused(args):
                 "workspace_gb": ws.numel() / 1e9,
                 "resident_gb": base_mem / 1e9,
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-                "variants": variants,
+                "variants": variants, "teacher_topk": topk,
                 "clocks": clk.summary(), "gpu_launches": launches, "device_status": status,
                 "kernel_digest": kernel_digest()}
         print(json.dumps(line), flush=True)

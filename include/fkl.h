@@ -148,6 +148,28 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
                                 void* dh, float* dW,
                                 void* ws, size_t ws_bytes, void* stream);
 
+/* ---- teacher top-K cache producer ------------------------------------------
+ * The offline step before the loss: z = h W^T for the TEACHER's hidden states h
+ * [N][d] (bf16) and LM head W [V][d] (bf16), and per row the K largest logits:
+ * idx [N][K] (int32) and logit [N][K] (fp32, the fp32-accumulated z), sorted by
+ * logit descending, equal logits by id ascending -- the cache of the teacher's
+ * top-100 per position of "Effektivnaya distillyatsiya znaniy" (malakhovai.ru,
+ * paragraph 2) and "Wissensdestillation mit deutlich weniger GPU-Speicher"
+ * (dailytechsnack.ch, section "Teacher-Ausgaben einmalig zwischenspeichern"),
+ * in the layout fkl_forward reads (its `idx` and `tlogit`).
+ * Two tensor-core passes per chunk of rows: the first keeps each row's max per
+ * 256-column vocabulary tile; theta = the K-th largest of those maxima is a lower
+ * bound of the row's K-th largest logit, and the logits above it lie in fewer
+ * than K tiles; the second pass recomputes the logits and keeps those >= theta;
+ * a last kernel selects and sorts the K largest.  Where more than K logits tie
+ * at theta itself, which of them are kept is unspecified.  The full N x V
+ * logits are never stored.  Conventions as above (device pointers, caller-owned,
+ * stream-ordered, status word at the start of ws); chunk = 0 means 1024 rows.
+ * The workspace is O(chunk * min(V, 256 K)) bytes: 208 MB at V = 201088, K = 100. */
+size_t fkl_topk_workspace_size(int64_t N, int d, int64_t V, int K, int chunk);
+fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int64_t V, int K, int chunk,
+                            int32_t* idx, float* logit, void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream` and returns the device status word of `ws` (FKL_OK if
  * no device-side error was recorded since the last call that used `ws`). */
 fkl_status fkl_get_status(const void* ws, void* stream);

@@ -33,6 +33,9 @@ SIGNATURES = {
     "fkl_forward_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_i64, c_int,
                                     c_i64, c_int, c_float, c_int, c_void_p, c_void_p, c_void_p,
                                     c_void_p]),
+    "fkl_topk_workspace_size": (c_size, [c_i64, c_int, c_i64, c_int, c_int]),
+    "fkl_teacher_topk": (c_int, [c_void_p, c_void_p, c_i64, c_int, c_i64, c_int, c_int, c_void_p, c_void_p,
+                                 c_void_p, c_size, c_void_p]),
     "fkl_get_status": (c_int, [c_void_p, c_void_p]),
     "fkl_status_string": (c_char_p, [c_int]),
     "fkl_last_error": (c_char_p, []),

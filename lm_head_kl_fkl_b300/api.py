@@ -143,6 +143,34 @@ def forward_backward(h, W, idx, tlogit, mask, T: float, grad_loss: Optional[torc
     return loss, lse, dh, dW
 
 
+def topk_workspace_size(N: int, d: int, V: int, K: int, chunk: int = 0) -> int:
+    n = _lib.lib().fkl_topk_workspace_size(int(N), int(d), int(V), int(K), int(chunk))
+    if n == 0:
+        raise ValueError(f"invalid sizes N={N} d={d} V={V} K={K} chunk={chunk}")
+    return int(n)
+
+
+def teacher_topk(h: torch.Tensor, W: torch.Tensor, K: int, chunk: int = 0,
+                 ws: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Teacher top-K cache: (idx [N,K] int32, logit [N,K] fp32), logits descending."""
+    _expect(h, "h", torch.bfloat16, 2)
+    dev = h.device
+    _expect(W, "W", torch.bfloat16, 2, dev)
+    N, d = h.shape
+    V, d2 = W.shape
+    if d2 != d:
+        raise ValueError(f"h is [N,{d}] but W is [V,{d2}]")
+    L = _lib.lib()
+    if ws is None:
+        ws = torch.empty(topk_workspace_size(N, d, V, K, chunk), dtype=torch.uint8, device=dev)
+    idx = torch.empty((N, K), dtype=torch.int32, device=dev)
+    logit = torch.empty((N, K), dtype=torch.float32, device=dev)
+    st = L.fkl_teacher_topk(_ptr(h), _ptr(W), N, d, V, int(K), int(chunk), _ptr(idx), _ptr(logit), _ptr(ws),
+                            ws.numel(), _stream(dev))
+    _check(st, "fkl_teacher_topk")
+    return idx, logit
+
+
 def get_status(ws: torch.Tensor) -> int:
     """Synchronises the current stream and returns the workspace's device status word."""
     return int(_lib.lib().fkl_get_status(_ptr(ws), _stream(ws.device)))
@@ -187,7 +215,7 @@ def profile_reset():
 def profile_read() -> dict:
     """{kernel name: (total ms, launches, algorithmic FLOP)} of the recorded launches."""
     L = _lib.lib()
-    n = 16
+    n = 64
     ms = (ctypes.c_double * n)()
     cnt = (ctypes.c_int64 * n)()
     fl = (ctypes.c_double * n)()

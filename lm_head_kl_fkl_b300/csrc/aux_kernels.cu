@@ -245,6 +245,168 @@ void launch_dz_from_logits(void* yz, int64_t Vs, int64_t V, const float* part_m,
                                                n_valid, grad, T, sidx, sp, K);
 }
 
+// ---------------------------------------------------------------- teacher top-K
+// Order-preserving map of a float onto uint32 (a < b  <=>  key(a) < key(b)).
+__device__ __forceinline__ uint32_t fkey(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unkey(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Per row (one warp): theta = the K-th largest of its per-tile maxima, or -inf
+// when there are fewer than K tiles.  At least K logits of the row are >= theta
+// (each of the K tiles contributes its max), and every logit > theta lies in one of
+// the < K tiles whose max exceeds theta, so at most (K - 1) * 256 logits are above
+// it.  Also clears the row's candidate counters.
+__global__ void topk_threshold_kernel(const float* __restrict__ part_m, int stride, int ntiles, int rows, int K,
+                                      float* __restrict__ theta, int* __restrict__ cnt_gt,
+                                      int* __restrict__ cnt_eq) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    float th = -INFINITY;
+    if (ntiles >= K) {
+        uint32_t t = 0;  // largest key with at least K tile maxima at or above it
+        for (int b = 31; b >= 0; --b) {
+            const uint32_t cand = t | (1u << b);
+            int c = 0;
+            for (int n = lane; n < ntiles; n += 32) c += fkey(part_m[static_cast<size_t>(n) * stride + r]) >= cand;
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            if (c >= K) t = cand;
+        }
+        th = unkey(t);
+    }
+    if (lane == 0) {
+        theta[r] = th;
+        cnt_gt[r] = 0;
+        cnt_eq[r] = 0;
+    }
+}
+
+// Per row (one block of 256): the K largest logits among the candidates, sorted by
+// value (descending), equal values by id (ascending).  If at least K candidates
+// are above theta, the K-th largest value is found by a bitwise search over the
+// order-preserving keys and the boundary ties are resolved by the smallest ids;
+// otherwise all of them are taken and the rest is filled with logits equal to
+// theta from the tie list.
+__global__ void topk_select_kernel(const float* __restrict__ cand_v, const int* __restrict__ cand_i, int cap,
+                                   const int* __restrict__ cnt_gt, const int* __restrict__ cnt_eq,
+                                   const int* __restrict__ tie_i, const float* __restrict__ theta, int K,
+                                   int32_t* __restrict__ idx_out, float* __restrict__ logit_out) {
+    __shared__ uint32_t s_key[kMaxK];
+    __shared__ int s_id[kMaxK];
+    __shared__ int s_n;
+    const int r = blockIdx.x;
+    const float* v = cand_v + static_cast<size_t>(r) * cap;
+    const int* id = cand_i + static_cast<size_t>(r) * cap;
+    const int n = min(cnt_gt[r], cap);
+    for (int k = threadIdx.x; k < kMaxK; k += blockDim.x) {
+        s_key[k] = 0u;  // below every real key: sorts last
+        s_id[k] = INT_MAX;
+    }
+    if (threadIdx.x == 0) s_n = 0;
+    __syncthreads();
+    if (n >= K) {
+        uint32_t t = 0;  // key of the K-th largest candidate
+        for (int b = 31; b >= 0; --b) {
+            const uint32_t cand = t | (1u << b);
+            int c = 0;
+            for (int i = threadIdx.x; i < n; i += blockDim.x) c += fkey(v[i]) >= cand;
+            if (__syncthreads_count(c > 0) == 0) continue;  // cheap exit: nobody reaches cand
+            __shared__ int s_cnt;
+            if (threadIdx.x == 0) s_cnt = 0;
+            __syncthreads();
+            if (c) atomicAdd(&s_cnt, c);
+            __syncthreads();
+            if (s_cnt >= K) t = cand;
+            __syncthreads();
+        }
+        int above = 0;  // candidates strictly above the K-th value
+        for (int i = threadIdx.x; i < n; i += blockDim.x) above += fkey(v[i]) > t;
+        __shared__ int s_above;
+        if (threadIdx.x == 0) s_above = 0;
+        __syncthreads();
+        if (above) atomicAdd(&s_above, above);
+        __syncthreads();
+        const int need = K - s_above;  // ties at the K-th value to keep, smallest ids first
+        uint32_t cut = 0;              // largest id bound with at most `need` ties below it ...
+        for (int b = 30; b >= 0; --b) {
+            const uint32_t c2 = cut | (1u << b);
+            int c = 0;
+            for (int i = threadIdx.x; i < n; i += blockDim.x) c += (fkey(v[i]) == t && static_cast<uint32_t>(id[i]) < c2);
+            __shared__ int s_c2;
+            if (threadIdx.x == 0) s_c2 = 0;
+            __syncthreads();
+            if (c) atomicAdd(&s_c2, c);
+            __syncthreads();
+            if (s_c2 < need) cut = c2;
+            __syncthreads();
+        }
+        // ... so the ties with id <= cut are exactly `need` of them
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const uint32_t kk = fkey(v[i]);
+            if (kk > t || (kk == t && static_cast<uint32_t>(id[i]) <= cut)) {
+                const int slot = atomicAdd(&s_n, 1);
+                if (slot < kMaxK) {
+                    s_key[slot] = kk;
+                    s_id[slot] = id[i];
+                }
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            s_key[i] = fkey(v[i]);
+            s_id[i] = id[i];
+        }
+        const int ne = min(cnt_eq[r], K - n);
+        const uint32_t tk = fkey(theta[r]);
+        for (int i = threadIdx.x; i < ne; i += blockDim.x) {
+            s_key[n + i] = tk;
+            s_id[n + i] = tie_i[static_cast<size_t>(r) * K + i];
+        }
+    }
+    __syncthreads();
+    // bitonic sort of the kMaxK slots: key descending, id ascending
+    for (int size = 2; size <= kMaxK; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < kMaxK; i += blockDim.x) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;
+                    const bool i_first = s_key[i] > s_key[j] || (s_key[i] == s_key[j] && s_id[i] < s_id[j]);
+                    if (i_first != desc) {
+                        const uint32_t tk = s_key[i];
+                        s_key[i] = s_key[j];
+                        s_key[j] = tk;
+                        const int ti = s_id[i];
+                        s_id[i] = s_id[j];
+                        s_id[j] = ti;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        idx_out[static_cast<size_t>(r) * K + k] = s_id[k];
+        logit_out[static_cast<size_t>(r) * K + k] = unkey(s_key[k]);
+    }
+}
+
+void launch_topk_threshold(const float* part_m, int part_stride, int ntiles, int rows, int K, float* theta,
+                           int* cnt_gt, int* cnt_eq, cudaStream_t s) {
+    topk_threshold_kernel<<<(rows + 7) / 8, 256, 0, s>>>(part_m, part_stride, ntiles, rows, K, theta, cnt_gt, cnt_eq);
+}
+
+void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const int* cnt_gt, const int* cnt_eq,
+                        const int* tie_i, const float* theta, int rows, int K, int32_t* idx_out, float* logit_out,
+                        cudaStream_t s) {
+    topk_select_kernel<<<rows, 256, 0, s>>>(cand_v, cand_i, cap, cnt_gt, cnt_eq, tie_i, theta, K, idx_out,
+                                            logit_out);
+}
+
 void launch_count_valid(const float* tlogit, const uint8_t* mask, int64_t N, int K, int* n_valid,
                         int grid, cudaStream_t s) {
     count_valid_kernel<<<grid, 256, 0, s>>>(tlogit, mask, N, K, n_valid);

@@ -88,6 +88,7 @@ const char* const kKindNames[KK_NUM] = {
     "count_valid", "teacher_prep", "fwd_gemm_lse", "fwd_finalize", "loss_reduce",
     "bwd_gemm_dz", "bwd_gemm_dh", "dh_reduce", "bwd_gemm_dw", "selftest_gemm",
     "fb_gemm_lse_keep", "fb_dz_from_logits",
+    "tk_gemm_tile_max", "tk_threshold", "tk_gemm_candidates", "tk_select",
 };
 
 // ---------------------------------------------------------------- device facts
@@ -267,6 +268,47 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
     // partials at once, so its partials share the dh partials' place.
     P.total = P.o_big + dz + std::max(part_fwd, part_dh);
     P.fwd_total = P.o_big + part_fwd;
+    return true;
+}
+
+// ---------------------------------------------------------------- teacher top-K plan
+constexpr int kDefaultTopkChunk = 1024;
+
+struct TopkPlan {
+    int64_t N, V, n_chunks;
+    int d, K, Cc, nt_v, cap;
+    size_t o_part, o_theta, o_gt, o_eq, o_cv, o_ci, o_tie, total;
+};
+
+bool make_topk_plan(int64_t N, int d, int64_t V, int K, int chunk, TopkPlan& P) {
+    if (check_sizes(N, d, V, K, chunk)) return false;
+    P.N = N;
+    P.d = d;
+    P.V = V;
+    P.K = K;
+    const int64_t want = chunk > 0 ? chunk : kDefaultTopkChunk;
+    P.Cc = static_cast<int>(std::min<int64_t>(want, cdiv(N, kBM) * kBM));
+    P.n_chunks = cdiv(N, P.Cc);
+    P.nt_v = static_cast<int>(cdiv(V, kVocabTile));
+    // logits above the threshold lie in fewer than K vocabulary tiles (or the
+    // threshold is -inf and there are fewer than K tiles in all)
+    P.cap = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(V, int64_t(std::max(K - 1, 1)) * kVocabTile)));
+    size_t off = 256;
+    P.o_part = off;
+    off += align256(size_t(P.nt_v) * P.Cc * 4);
+    P.o_theta = off;
+    off += align256(size_t(P.Cc) * 4);
+    P.o_gt = off;
+    off += align256(size_t(P.Cc) * 4);
+    P.o_eq = off;
+    off += align256(size_t(P.Cc) * 4);
+    P.o_cv = off;
+    off += align256(size_t(P.Cc) * P.cap * 4);
+    P.o_ci = off;
+    off += align256(size_t(P.Cc) * P.cap * 4);
+    P.o_tie = off;
+    off += align256(size_t(P.Cc) * K * 4);
+    P.total = off;
     return true;
 }
 
@@ -684,6 +726,72 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
             return st;
     }
     FKL_SMALL(KK_LOSS_REDUCE, launch_loss_reduce(rowloss, N, n_valid, T, loss, s));
+    return FKL_OK;
+}
+
+size_t fkl_topk_workspace_size(int64_t N, int d, int64_t V, int K, int chunk) {
+    TopkPlan P;
+    return make_topk_plan(N, d, V, K, chunk, P) ? P.total : 0;
+}
+
+fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int64_t V, int K, int chunk,
+                            int32_t* idx, float* logit, void* ws, size_t ws_bytes, void* stream) {
+    g_err[0] = 0;
+    if (!h || !W || !idx || !logit || !ws) return fail(FKL_ERR_INVALID_ARG, "null pointer");
+    if (const char* e = check_sizes(N, d, V, K, chunk)) return fail(FKL_ERR_INVALID_ARG, "%s", e);
+    if (!aligned16(h) || !aligned16(W) || !aligned16(ws))
+        return fail(FKL_ERR_INVALID_ARG, "h, W and ws must be 16-byte aligned");
+    TopkPlan P;
+    make_topk_plan(N, d, V, K, chunk, P);
+    if (ws_bytes < P.total)
+        return fail(FKL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, P.total);
+    if (fkl_status st = device_ready()) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* w = static_cast<char*>(ws);
+    int* status = reinterpret_cast<int*>(w);
+    float* part = reinterpret_cast<float*>(w + P.o_part);
+    float* theta = reinterpret_cast<float*>(w + P.o_theta);
+    int* cnt_gt = reinterpret_cast<int*>(w + P.o_gt);
+    int* cnt_eq = reinterpret_cast<int*>(w + P.o_eq);
+    float* cand_v = reinterpret_cast<float*>(w + P.o_cv);
+    int* cand_i = reinterpret_cast<int*>(w + P.o_ci);
+    int* tie_i = reinterpret_cast<int*>(w + P.o_tie);
+    FKL_CUDA_TRY(cudaMemsetAsync(w, 0, 256, s));
+
+    CUtensorMap tmW;
+    FKL_TMAP(tmW, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, kVocabTile / 2);
+    for (int64_t c = 0; c < P.n_chunks; ++c) {
+        const int64_t row0 = c * P.Cc;
+        const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
+        const double flop = 2.0 * rows * double(d) * double(V);
+        CUtensorMap tmH;
+        FKL_TMAP(tmH, BF16, static_cast<const char*>(h) + size_t(row0) * d * 2, uint64_t(d), uint64_t(rows),
+                 uint64_t(d) * 2, 64, 128);
+        GemmParams p{};
+        p.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
+        p.n_tiles = P.nt_v;
+        p.splits = 1;
+        p.kb_total = static_cast<int>(cdiv(d, kBK));
+        p.m_fastest = 1;
+        p.M = rows;
+        p.Ncols = static_cast<int>(V);
+        p.status = status;
+        p.part_m = part;
+        p.part_stride = P.Cc;
+        p.K = K;
+        if (fkl_status st = run_gemm(KK_TK_GEMM_TMAX, 256, 0, 0, EPI_TMAX, tmH, tmW, tmW, p, flop, s)) return st;
+        FKL_SMALL(KK_TK_THRESHOLD, launch_topk_threshold(part, P.Cc, P.nt_v, rows, K, theta, cnt_gt, cnt_eq, s));
+        p.theta = theta;
+        p.cnt_gt = cnt_gt;
+        p.cnt_eq = cnt_eq;
+        p.cand_v = cand_v;
+        p.cand_i = cand_i;
+        p.cand_cap = P.cap;
+        p.tie_i = tie_i;
+        if (fkl_status st = run_gemm(KK_TK_GEMM_CAND, 256, 0, 0, EPI_CAND, tmH, tmW, tmW, p, flop, s)) return st;
+        FKL_SMALL(KK_TK_SELECT, launch_topk_select(cand_v, cand_i, P.cap, cnt_gt, cnt_eq, tie_i, theta, rows, K,
+                                                   idx + size_t(row0) * K, logit + size_t(row0) * K, s));
+    }
     return FKL_OK;
 }
 

@@ -32,10 +32,18 @@ enum KernelKind {
     KK_SELFTEST,
     KK_FB_GEMM_LSE_Y,  // tcgen05 GEMM z = h W^T, logsumexp / gather epilogue that also keeps the logits
     KK_FB_DZ,          // dz from the kept logits (elementwise)
+    KK_TK_GEMM_TMAX,   // teacher top-K: tcgen05 GEMM, per-row max of each vocabulary tile
+    KK_TK_THRESHOLD,   // teacher top-K: per-row K-th largest tile max
+    KK_TK_GEMM_CAND,   // teacher top-K: tcgen05 GEMM again, logits >= threshold appended per row
+    KK_TK_SELECT,      // teacher top-K: per-row selection and sort of the candidates
     KK_NUM
 };
 
-enum Epilogue { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_LSE_Y = 3 };
+enum Epilogue { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_LSE_Y = 3, EPI_TMAX = 4, EPI_CAND = 5 };
+
+// Epilogues that stage a tile in shared memory for a TMA store (the others write
+// a few values per row with plain stores).
+constexpr bool epi_staged(int epi) { return epi == EPI_DZ || epi == EPI_F32 || epi == EPI_LSE_Y; }
 
 // Parameters of one persistent GEMM launch.  The unit space is
 // m_tiles (of 256 rows) x n_tiles (of BN columns) x splits; unit u maps to (m, n, s) with s slowest and either
@@ -63,6 +71,14 @@ struct GemmParams {
     // EPI_F32
     int split_row_stride;  // output row offset per split (dh partials), 0 otherwise
     int reduce;            // 1: TMA reduce-add into the output, 0: TMA store
+    // EPI_TMAX writes part_m ([n_tiles][part_stride], raw logits).  EPI_CAND:
+    const float* theta;    // [M] per-row threshold
+    int* cnt_gt;           // [M] logits > theta seen so far
+    int* cnt_eq;           // [M] logits == theta seen so far
+    float* cand_v;         // [M][cand_cap] values of the logits > theta
+    int* cand_i;           // [M][cand_cap] their vocabulary ids
+    int cand_cap;
+    int* tie_i;            // [M][K] ids of the first K logits == theta
 };
 
 // Launch helpers implemented in gemm_tc.cu.  Return cudaSuccess or the launch error.
@@ -86,6 +102,11 @@ void launch_loss_reduce(const float* rowloss, int64_t N, const int* n_valid, flo
                         cudaStream_t s);
 void launch_dh_reduce(const float* part, int splits, size_t split_elems, int rows, int d, void* dh,
                       cudaStream_t s);
+void launch_topk_threshold(const float* part_m, int part_stride, int ntiles, int rows, int K, float* theta,
+                           int* cnt_gt, int* cnt_eq, cudaStream_t s);
+void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const int* cnt_gt, const int* cnt_eq,
+                        const int* tie_i, const float* theta, int rows, int K, int32_t* idx_out, float* logit_out,
+                        cudaStream_t s);
 void launch_dz_from_logits(void* yz, int64_t Vs, int64_t V, const float* part_m, int part_stride,
                            const float* lse, const uint8_t* valid, const int* n_valid, const float* grad,
                            float T, const int* sidx, const float* sp, int K, int rows, cudaStream_t s);

@@ -39,6 +39,10 @@
 //   EPI_DZ   the same logits recomputed: dz = coef * (2^(z log2e/T - lse log2e) - s)
 //            in bf16, staged per warp in swizzled shared memory and TMA-stored.
 //   EPI_F32  plain fp32 tile, TMA-stored or TMA reduce-added (dh partials, dW).
+//   EPI_TMAX each row's largest logit over the tile (teacher top-K, first pass).
+//   EPI_CAND every logit >= the row's threshold, appended to the row's candidate
+//            list with an atomic counter (teacher top-K, second pass); logits
+//            equal to the threshold go to a separate list of at most K ids.
 //   EPI_LSE_Y  EPI_LSE for a forward whose backward follows at once: a first
 //            pass over the tile finds each row's tile max (and gathers the
 //            teacher logits), a second sums 2^(y) and keeps y = z log2e / T - max
@@ -65,8 +69,8 @@ struct PairCfg {
     static constexpr uint32_t B_SUB_BYTES = B_MN ? B_BOXES * 8192u : static_cast<uint32_t>(BNH) * 128u;
     static constexpr uint32_t B_BYTES = NSUB * B_SUB_BYTES;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t STAGING_BYTES = EPI == EPI_LSE ? 0u : 4u * 2u * 4096u;  // 2 x 4 KB per epilogue warp
-    static constexpr uint32_t RING_BUDGET = 196608u + (EPI == EPI_LSE ? 32768u : 0u);
+    static constexpr uint32_t STAGING_BYTES = epi_staged(EPI) ? 4u * 2u * 4096u : 0u;  // 2 x 4 KB per epilogue warp
+    static constexpr uint32_t RING_BUDGET = 196608u + (epi_staged(EPI) ? 0u : 32768u);
     static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) > 8 ? 8 : (RING_BUDGET / STAGE_BYTES);
     static constexpr uint32_t BAR_BYTES = 256;
     static constexpr size_t SMEM = size_t(STAGES) * STAGE_BYTES + STAGING_BYTES + BAR_BYTES + 1024;
@@ -187,7 +191,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (EPI != EPI_LSE) tma_prefetch_desc(&tmOut);
+        if (epi_staged(EPI)) tma_prefetch_desc(&tmOut);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(s_tmem), 512);
@@ -459,6 +463,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     p.part_l[o] = l0 + l1;
                     p.part_g[o] = g;
                 }
+            } else if constexpr (EPI == EPI_TMAX) {
+                if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
+                tc_fence_after();
+                const int v0 = n * BN;
+                float mt = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int col0 = v0 + c * 32;
+                    if (col0 >= p.Ncols) break;
+                    float z[32];
+                    __syncwarp();
+                    tmem_ld32(tt + c * 32, z);
+                    const int nv = p.Ncols - col0;
+                    float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        cm0 = fmaxf(cm0, (j < nv) ? z[j] : -INFINITY);
+                        cm1 = fmaxf(cm1, (j + 1 < nv) ? z[j + 1] : -INFINITY);
+                    }
+                    mt = fmaxf(mt, fmaxf(cm0, cm1));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
+                if (row_ok) p.part_m[static_cast<size_t>(n) * p.part_stride + row] = mt;
+            } else if constexpr (EPI == EPI_CAND) {
+                const float th = row_ok ? p.theta[row] : INFINITY;
+                if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
+                tc_fence_after();
+                const int v0 = n * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int col0 = v0 + c * 32;
+                    if (col0 >= p.Ncols) break;
+                    float z[32];
+                    __syncwarp();
+                    tmem_ld32(tt + c * 32, z);
+                    const int nv = p.Ncols - col0;
+                    uint32_t hit = 0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) hit |= (j < nv && z[j] >= th) ? (1u << j) : 0u;
+                    while (hit) {  // rare: about K logits per row pass the threshold over the whole vocabulary
+                        const int j = __ffs(hit) - 1;
+                        hit &= hit - 1;
+                        const float v = select32(z, j);
+                        if (v > th) {
+                            const int slot = atomicAdd(p.cnt_gt + row, 1);
+                            if (slot < p.cand_cap) {
+                                p.cand_v[static_cast<size_t>(row) * p.cand_cap + slot] = v;
+                                p.cand_i[static_cast<size_t>(row) * p.cand_cap + slot] = col0 + j;
+                            }
+                        } else {
+                            const int slot = atomicAdd(p.cnt_eq + row, 1);
+                            if (slot < p.K) p.tie_i[static_cast<size_t>(row) * p.K + slot] = col0 + j;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
             } else if constexpr (EPI == EPI_DZ) {
                 const int v0 = n * BN;
                 TeacherCursor cur;
@@ -547,7 +611,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
             }
         }
-        if (EPI != EPI_LSE && lane == 0) bulk_wait_all();
+        if (epi_staged(EPI) && lane == 0) bulk_wait_all();
         __syncwarp();
     }
 
@@ -594,6 +658,7 @@ size_t gemm_smem_bytes(int bn, int b_mn, int epi) {
 #define FKL_SMEM_CASE(BN_, NS_, B_, E_) \
     if (bn == BN_ * NS_ && b_mn == B_ && epi == E_) return PairCfg<BN_, NS_, B_, E_>::SMEM;
     FKL_SMEM_CASE(256, 1, 0, EPI_LSE) FKL_SMEM_CASE(256, 1, 0, EPI_DZ) FKL_SMEM_CASE(256, 1, 0, EPI_LSE_Y)
+    FKL_SMEM_CASE(256, 1, 0, EPI_TMAX) FKL_SMEM_CASE(256, 1, 0, EPI_CAND)
     FKL_SMEM_CASE(256, 2, 0, EPI_F32) FKL_SMEM_CASE(256, 2, 1, EPI_F32)
     FKL_SMEM_CASE(256, 1, 0, EPI_F32) FKL_SMEM_CASE(256, 1, 1, EPI_F32)
     FKL_SMEM_CASE(192, 1, 0, EPI_F32) FKL_SMEM_CASE(192, 1, 1, EPI_F32)
@@ -613,6 +678,16 @@ cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& 
     if (epi == EPI_DZ) {
         if (bn == 256 && a_mn == 0 && b_mn == 0)
             return launch_one<256, 1, 0, 0, EPI_DZ>(tmA, tmB, tmOut, p, max_pairs, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (epi == EPI_TMAX) {
+        if (bn == 256 && a_mn == 0 && b_mn == 0)
+            return launch_one<256, 1, 0, 0, EPI_TMAX>(tmA, tmB, tmOut, p, max_pairs, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (epi == EPI_CAND) {
+        if (bn == 256 && a_mn == 0 && b_mn == 0)
+            return launch_one<256, 1, 0, 0, EPI_CAND>(tmA, tmB, tmOut, p, max_pairs, stream);
         return cudaErrorInvalidValue;
     }
     if (epi == EPI_LSE_Y) {

@@ -39,6 +39,7 @@ _SIGS = {
     "fklo_rows": [_d, _d, _i32, _d, _u8, _L, _L, _L, _L, _F, _F, _i64p, _L, _I, _d, _d, _d, _i64p],
     "fklo_dW_rows": [_d, _d, _i32, _d, _u8, _L, _L, _L, _L, _F, _F, _d, _i64p, _L, _I, _d],
     "fklo_student_lse": [_d, _d, _L, _L, _L, _F, _I, _d],
+    "fklo_teacher_topk": [_d, _d, _L, _L, _L, _L, _I, _i64p, _d],
 }
 
 
@@ -155,6 +156,23 @@ class CppOracle:
         out = np.empty(N)
         self.lib.fklo_student_lse(_p(h, _d), _p(W, _d), N, d, W.shape[0], float(T), threads(), _p(out, _d))
         return out
+
+
+def _teacher_topk(self, h, W, K, rows=None, row_block=256):
+    """Per row the K largest logits (descending, ties by ascending id): (idx, logit, None)."""
+    del row_block
+    h, W = _f64(h), _f64(W)
+    if rows is not None:
+        h = np.ascontiguousarray(h[np.asarray(rows, dtype=np.int64)])
+    N, d = h.shape
+    V = W.shape[0]
+    idx = np.empty((N, K), dtype=np.int64)
+    val = np.empty((N, K))
+    self.lib.fklo_teacher_topk(_p(h, _d), _p(W, _d), N, d, V, int(K), threads(), _p(idx, _i64p), _p(val, _d))
+    return idx, val, None
+
+
+CppOracle.teacher_topk = _teacher_topk
 
 
 def load() -> CppOracle:

@@ -32,6 +32,7 @@
 // so results do not depend on the thread count or on row_block.
 #include <algorithm>
 #include <cmath>
+#include <numeric>
 #include <cstdint>
 #include <limits>
 #include <thread>
@@ -251,6 +252,28 @@ void fklo_dW_rows(const double* h, const double* W, const int32_t* idx, const do
                     if (idx[i * K + k] == v) s += p[k];
                 const double c = grad_loss * T / static_cast<double>(nv) * (std::exp(z / T - lse[i]) - s);
                 for (int64_t j = 0; j < d; ++j) o[j] += c * h[i * d + j];
+            }
+        }
+    });
+}
+
+// Teacher cache: per row the K largest logits (descending, equal logits by
+// ascending id) and their ids; idx [N][K], val [N][K].  The top-100 per position
+// of "Effektivnaya distillyatsiya znaniy" (malakhovai.ru, paragraph 2).
+void fklo_teacher_topk(const double* h, const double* W, int64_t N, int64_t d, int64_t V, int64_t K, int threads,
+                       int64_t* idx, double* val) {
+    parallel_for(N, threads, [&](int64_t b, int64_t e) {
+        std::vector<double> z(static_cast<size_t>(V));
+        std::vector<int64_t> ord(static_cast<size_t>(V));
+        for (int64_t i = b; i < e; ++i) {
+            logit_row(h + i * d, W, d, V, z.data());
+            std::iota(ord.begin(), ord.end(), int64_t(0));
+            std::partial_sort(ord.begin(), ord.begin() + K, ord.end(), [&](int64_t a, int64_t c) {
+                return z[a] > z[c] || (z[a] == z[c] && a < c);
+            });
+            for (int64_t k = 0; k < K; ++k) {
+                idx[i * K + k] = ord[k];
+                val[i * K + k] = z[ord[k]];
             }
         }
     });

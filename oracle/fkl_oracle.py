@@ -38,7 +38,7 @@ import numpy as np
 
 __all__ = [
     "teacher_distribution", "row_valid", "student_lse", "forward", "backward",
-    "rows_forward_backward", "dW_rows", "kl_rows_from_logits",
+    "rows_forward_backward", "dW_rows", "kl_rows_from_logits", "teacher_topk",
 ]
 
 
@@ -202,3 +202,29 @@ def dW_rows(h, W, idx, tlogit, mask, T, lse, vocab_rows, grad_loss=1.0, row_bloc
         coef = valid[r0:r1].astype(np.float64) * float(grad_loss) * float(T) / n_valid
         out += (coef[:, None] * (q - s)).T @ hb
     return out
+
+
+def teacher_topk(h, W, K, rows=None, row_block=256):
+    """The teacher cache: per row the K largest logits z = h W^T (fp64) and their ids.
+
+    Ordered by logit descending, equal logits by id ascending -- the top-100 per
+    position that "Effektivnaya distillyatsiya znaniy" (malakhovai.ru, paragraph 2)
+    and "Wissensdestillation mit deutlich weniger GPU-Speicher" (dailytechsnack.ch,
+    section "Teacher-Ausgaben einmalig zwischenspeichern") cache once, offline.
+    `rows` restricts the computation to those rows.  Returns (idx [n,K] int64,
+    logit [n,K] fp64, z_full [n,V] fp64 of the same rows).
+    """
+    W = np.asarray(W, dtype=np.float64)
+    rows = np.arange(h.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    idx = np.empty((len(rows), K), dtype=np.int64)
+    val = np.empty((len(rows), K))
+    zs = np.empty((len(rows), W.shape[0]))
+    for b0 in range(0, len(rows), row_block):
+        rb = rows[b0:b0 + row_block]
+        z = np.asarray(h[rb], dtype=np.float64) @ W.T
+        # sort key: logit descending, then id ascending (a stable sort of -z keeps ids ascending)
+        order = np.argsort(-z, axis=1, kind="stable")[:, :K]
+        idx[b0:b0 + len(rb)] = order
+        val[b0:b0 + len(rb)] = np.take_along_axis(z, order, axis=1)
+        zs[b0:b0 + len(rb)] = z
+    return idx, val, zs

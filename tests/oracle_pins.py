@@ -249,9 +249,46 @@ def pin_sampled_helpers(orc):
     np.testing.assert_allclose(orc.student_lse(h, W, 1.5, row_block=9), full["lse"], rtol=1e-14)
 
 
+# (T1) Teacher cache, closed form: with W = I (d = V) the logits are h itself, so
+# the cache is the K largest entries of each h row -- numpy's stable argsort of -h.
+def pin_topk_identity_head(orc):
+    rng = np.random.default_rng(53)
+    V = 300
+    h = rng.standard_normal((9, V))
+    for K in (1, 7, 100, V):
+        idx, val, _ = orc.teacher_topk(h, np.eye(V), K)
+        ref = np.argsort(-h, axis=1, kind="stable")[:, :K]
+        assert np.array_equal(idx, ref)
+        np.testing.assert_array_equal(val, np.take_along_axis(h, ref, axis=1))
+
+
+# (T2) Ties go to the smaller id, and the order is by logit first: duplicated
+# vocabulary rows give equal logits; a permutation of W's rows permutes the ids.
+def pin_topk_ties_and_permutation(orc):
+    rng = np.random.default_rng(59)
+    d, V, K = 6, 50, 12
+    h = rng.standard_normal((5, d))
+    W = rng.standard_normal((V, d))
+    W[30] = W[4]
+    W[41] = W[4]
+    W[17] = W[2]
+    idx, val, _ = orc.teacher_topk(h, W, V)
+    assert np.all(np.diff(val, axis=1) <= 0)
+    for i in range(5):
+        pos = {int(v): k for k, v in enumerate(idx[i])}
+        assert pos[4] < pos[30] < pos[41] and pos[2] < pos[17]
+        assert val[i, pos[4]] == val[i, pos[41]]
+    perm = rng.permutation(V)
+    idx_p, val_p, _ = orc.teacher_topk(h, W[perm], K)
+    z = h @ W.T
+    for i in range(5):  # the same K logits; each id names the permuted row it came from
+        np.testing.assert_allclose(val_p[i], val[i, :K], rtol=1e-14)
+        np.testing.assert_allclose(val_p[i], z[i, perm[idx_p[i]]], rtol=1e-14)
+
+
 ALL_PINS = [
     pin_kl_nonnegative, pin_zero_case, pin_chunk_invariance, pin_bias_shift,
     pin_finite_differences, pin_k1_cross_entropy, pin_autograd_general_k, pin_zero_sum,
     pin_uniform_student, pin_lse_library, pin_page_soft_labels, pin_degenerate_rows,
-    pin_sampled_helpers,
+    pin_sampled_helpers, pin_topk_identity_head, pin_topk_ties_and_permutation,
 ]

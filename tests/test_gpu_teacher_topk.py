@@ -1,0 +1,121 @@
+"""The teacher top-K cache producer (fkl_teacher_topk) against the fp64 oracle.
+
+The GPU ranks fp32 tensor-core logits and the oracle fp64 ones, so near-equal
+logits may rank differently; what is unique is checked exactly and the rest for
+validity: ids distinct and in range, logits sorted (equal logits by id), each
+returned logit equal to the oracle's logit at that id within the fp32 error, no
+unselected logit above the selected ones (beyond that error), and the selected set
+equal to the oracle's wherever the oracle's K-th and (K+1)-th logits are apart.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lm_head_kl_fkl_b300 import api, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(a_f32):
+    return synth.f32_to_bf16_bits(np.asarray(a_f32, dtype=np.float32))
+
+
+def _run(h_bits, W_bits, K, chunk=0):
+    h = torch.from_numpy(h_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    W = torch.from_numpy(W_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    idx, logit = api.teacher_topk(h, W, K, chunk)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy().astype(np.int64), logit.cpu().numpy().astype(np.float64)
+
+
+def _check(h_bits, W_bits, K, idx, val, rows=None, tol_abs=2e-4, tol_rel=2e-5):
+    hf, Wf = synth.bf16_bits_to_f64(h_bits), synth.bf16_bits_to_f64(W_bits)
+    rows = np.arange(hf.shape[0]) if rows is None else np.asarray(rows)
+    o_idx, o_val, z = oracle.teacher_topk(hf, Wf, K, rows)
+    V = Wf.shape[0]
+    for r, i in enumerate(rows):
+        gi, gv, zi = idx[i], val[i], z[r]
+        assert np.all((gi >= 0) & (gi < V)) and len(set(gi.tolist())) == K
+        assert np.all(np.diff(gv) <= 0)
+        eq = np.diff(gv) == 0
+        assert np.all(np.diff(gi)[eq] > 0), "equal logits must be ordered by id"
+        tol = tol_abs + tol_rel * np.abs(zi).max()
+        assert np.abs(gv - zi[gi]).max() <= tol
+        sel = np.zeros(V, bool)
+        sel[gi] = True
+        if K < V:
+            assert zi[~sel].max() <= zi[sel].min() + 2 * tol
+            if o_val[r, K - 1] - np.sort(zi)[::-1][K] > 2 * tol:
+                assert set(gi.tolist()) == set(o_idx[r].tolist())
+
+
+CASES = [
+    # N, d, V, K: threshold path (tiles >= K), ragged everywhere
+    (300, 256, 5000, 16),
+    (257, 136, 32768, 100),
+    # fewer vocabulary tiles than K: every logit is a candidate
+    (300, 256, 5000, 100),
+    (130, 64, 777, 1),
+    (64, 64, 256, 256),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "N{}_d{}_V{}_K{}".format(*c))
+def test_topk_against_oracle(case):
+    N, d, V, K = case
+    rng = np.random.default_rng(7000 + N + K)
+    h = _bf16(rng.standard_normal((N, d)))
+    W = _bf16(rng.standard_normal((V, d)) / np.sqrt(d))
+    idx, val = _run(h, W, K, chunk=128 if N > 200 else 0)
+    _check(h, W, K, idx, val)
+
+
+def test_exact_ties_from_repeated_vocabulary_rows():
+    rng = np.random.default_rng(7100)
+    N, d, V, K = 96, 128, 4096, 64
+    Wf = rng.standard_normal((V, d)) / np.sqrt(d)
+    Wf[1000:1400] = Wf[0:400]  # every logit of ids 0..399 appears twice
+    h, W = _bf16(rng.standard_normal((N, d))), _bf16(Wf)
+    idx, val = _run(h, W, K)
+    _check(h, W, K, idx, val)
+    a, b = _run(h, W, K)
+    assert np.array_equal(a, idx) and np.array_equal(b, val)  # deterministic
+
+
+def test_all_logits_equal():
+    N, d, V, K = 40, 64, 3000, 10
+    h = _bf16(np.random.default_rng(7200).standard_normal((N, d)))
+    W = _bf16(np.zeros((V, d)))
+    idx, val = _run(h, W, K)
+    assert np.all(val == 0.0)
+    for i in range(N):
+        assert len(set(idx[i].tolist())) == K and np.all(np.diff(idx[i]) > 0)
+
+
+def test_cache_feeds_the_loss():
+    """The producer's output is the loss's teacher input as it stands."""
+    rng = np.random.default_rng(7300)
+    N, d, V, K, T = 200, 96, 2048, 32, 2.0
+    ht, Wt = _bf16(rng.standard_normal((N, 64))), _bf16(rng.standard_normal((V, 64)) / 8.0)
+    idx, val = _run(ht, Wt, K)
+    hs, Ws = _bf16(rng.standard_normal((N, d))), _bf16(rng.standard_normal((V, d)) / np.sqrt(d))
+    x = dict(h=hs, W=Ws, idx=idx.astype(np.int32), t=val.astype(np.float32),
+             mask=np.ones(N, np.uint8), T=T)
+    dev = torch.device("cuda")
+    loss, lse = api.forward(torch.from_numpy(hs.view(np.int16)).view(torch.bfloat16).to(dev),
+                            torch.from_numpy(Ws.view(np.int16)).view(torch.bfloat16).to(dev),
+                            torch.from_numpy(x["idx"]).to(dev), torch.from_numpy(x["t"]).to(dev),
+                            torch.from_numpy(x["mask"]).to(dev), T)
+    ref = oracle.forward(synth.bf16_bits_to_f64(hs), synth.bf16_bits_to_f64(Ws), x["idx"], x["t"], x["mask"], T)
+    assert abs(loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"])
+
+
+def test_full_size_teacher_cache_rows():
+    """gpt-oss-20b-like head (d = 2880, V = 201088, K = 100) at the producer's
+    default chunk, 2048 tokens; 64 sampled rows against the oracle."""
+    x = synth.config_inputs(3)
+    N = 2048
+    idx, val = _run(x["h"][:N], x["W"], 100)
+    rows = np.sort(np.random.default_rng(7400).choice(N, 64, replace=False))
+    _check(x["h"][:N], x["W"], 100, idx, val, rows=rows)

@@ -77,6 +77,10 @@ MUTATIONS = {
     "dW_transposed_operand": ("dW += dz.T @ h[r0:r1]", "dW += (dz.T @ h[r0:r1])[::-1]"),
     "lse_missing_max_shift": ("return m + np.log(np.exp(a - m[:, None]).sum(axis=1))",
                               "return np.log(np.exp(a - m[:, None]).sum(axis=1))"),
+    "topk_ascending": ('order = np.argsort(-z, axis=1, kind="stable")[:, :K]',
+                       'order = np.argsort(z, axis=1, kind="stable")[:, :K]'),
+    "topk_ties_to_larger_id": ('order = np.argsort(-z, axis=1, kind="stable")[:, :K]',
+                               'order = (z.shape[1] - 1 - np.argsort(-z[:, ::-1], axis=1, kind="stable"))[:, :K]'),
 }
 
 # The same kinds of mistake, planted in the C++ oracle's source.
@@ -96,6 +100,10 @@ CPP_MUTATIONS = {
     "dW_rows_permuted": ("double* dwv = dW + v * d;", "double* dwv = dW + (V - 1 - v) * d;"),
     "lse_missing_max_shift": ("return m + std::log(s);", "return std::log(s);"),
     "dh_wrong_weight_row": ("dhi[j] += dzr[v] * W[v * d + j];", "dhi[j] += dzr[v] * W[((v + 1) % V) * d + j];"),
+    "topk_ascending": ("return z[a] > z[c] || (z[a] == z[c] && a < c);",
+                       "return z[a] < z[c] || (z[a] == z[c] && a < c);"),
+    "topk_ties_to_larger_id": ("return z[a] > z[c] || (z[a] == z[c] && a < c);",
+                               "return z[a] > z[c] || (z[a] == z[c] && a > c);"),
 }
 
 
