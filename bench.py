@@ -328,6 +328,29 @@ def run_fused(args):
                     "passes instead of recomputed (6 N d V tensor FLOP)",
             "device_status": api.get_status(ws)}}
 
+        # the KL + hard-label cross-entropy mixture (alpha = 0.5) through its own entry points
+        label = torch.from_numpy(np.random.default_rng(11).integers(0, V, N).astype(np.int32)).to(dev)
+
+        def step_mix():
+            _, ls, l1 = api.mix_forward(h, W, idx, t, mask, label, T, 0.5, chunk=args.chunk, ws=ws)
+            api.mix_backward(h, W, idx, t, mask, label, T, 0.5, ls, l1, chunk=args.chunk, ws=ws)
+
+        for _ in range(2):
+            step_mix()
+        torch.cuda.synchronize()
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for _ in range(args.steps):
+            step_mix()
+        m1.record(stream)
+        torch.cuda.synchronize()
+        mstep = m0.elapsed_time(m1) / args.steps
+        variants["kl_ce_mixture"] = {
+            "value": N / (mstep / 1e3), "unit": "tokens/s (this rank)", "ms_per_step": mstep,
+            "tflops_8NdV": flop_step / (mstep / 1e3) / 1e12, "alpha": 0.5,
+            "what": "fkl_mix_forward + fkl_mix_backward: alpha T^2 KL + (1 - alpha) CE on a hard label",
+            "device_status": api.get_status(ws)}
+
     # ---- the teacher top-K cache producer on the same shapes (h, W standing in for the teacher's)
     topk = None
     if not args.no_variants:

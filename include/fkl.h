@@ -127,6 +127,31 @@ fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const 
                         void* dh, float* dW,
                         void* ws, size_t ws_bytes, void* stream);
 
+/* KL + hard-label cross-entropy mixture.  "Distillyatsiya i szhatie modeley"
+ * (ml-book.com, section "Kak eto rabotaet: myagkie metki i temperatura") has the
+ * student's loss mix the KL between the softened distributions with the ordinary
+ * cross-entropy on the true labels, the T^2 factor keeping the KL gradients in
+ * scale; the weighting formula itself is lost from the page and is read as the
+ * usual convex mix:
+ *   loss  = alpha T^2 mean KL_i + (1 - alpha) mean CE_i     (means over valid rows)
+ *   CE_i  = lse1_i - z_{i,label_i},  lse1_i = logsumexp_v z_iv  (temperature 1)
+ *   dz_iv = g valid_i [alpha T (q_iv - s_iv) + (1 - alpha)(q1_iv - [v = label_i])] / N_valid,
+ *           q1 = exp(z - lse1)
+ * label [N] int32, in [0, V) for every valid row (FKL_ERR_INDEX in the status
+ * word otherwise); 0 <= alpha <= 1 (alpha = 1 is the plain loss of fkl_forward /
+ * fkl_backward).  lse1 [N] fp32 is written by the forward and read by the
+ * backward.  Everything else as in fkl_forward / fkl_backward, with the same
+ * workspace.  Costs one more exponential per logit in each pass. */
+fkl_status fkl_mix_forward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                           const uint8_t* mask, const int32_t* label, int64_t N, int d, int64_t V, int K,
+                           float T, float alpha, int chunk, float* loss, float* lse, float* lse1,
+                           void* ws, size_t ws_bytes, void* stream);
+fkl_status fkl_mix_backward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                            const uint8_t* mask, const int32_t* label, int64_t N, int d, int64_t V, int K,
+                            float T, float alpha, int chunk, const float* lse, const float* lse1,
+                            const float* grad_loss, void* dh, float* dW,
+                            void* ws, size_t ws_bytes, void* stream);
+
 /* Forward and backward in one call, for a training step that needs the loss
  * gradient at once (the upstream gradient is known before the call; grad_loss
  * NULL = 1.0).  Writes what fkl_forward followed by fkl_backward write: loss,

@@ -27,6 +27,12 @@ SIGNATURES = {
     "fkl_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_i64, c_int, c_i64,
                              c_int, c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_size, c_void_p]),
+    "fkl_mix_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_i64, c_int,
+                                c_i64, c_int, c_float, c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_size, c_void_p]),
+    "fkl_mix_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_i64, c_int,
+                                 c_i64, c_int, c_float, c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                 c_void_p, c_void_p, c_size, c_void_p]),
     "fkl_forward_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_i64, c_int,
                                      c_i64, c_int, c_float, c_int, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_void_p, c_size, c_void_p]),

@@ -120,6 +120,43 @@ def backward(h, W, idx, tlogit, mask, T: float, lse: torch.Tensor,
     return dh, dW
 
 
+def mix_forward(h, W, idx, tlogit, mask, label, T: float, alpha: float, chunk: int = 0,
+                ws: Optional[torch.Tensor] = None):
+    """KL + hard-label CE mixture, forward: (loss [1], lse [N], lse1 [N]) fp32."""
+    N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
+    _expect(label, "label", torch.int32, 1, dev)
+    if ws is None:
+        ws = alloc_workspace(N, d, V, K, chunk, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    lse1 = torch.empty(N, dtype=torch.float32, device=dev)
+    st = _lib.lib().fkl_mix_forward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), _ptr(label), N, d, V,
+                                    K, float(T), float(alpha), int(chunk), _ptr(loss), _ptr(lse), _ptr(lse1),
+                                    _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "fkl_mix_forward")
+    return loss, lse, lse1
+
+
+def mix_backward(h, W, idx, tlogit, mask, label, T: float, alpha: float, lse, lse1,
+                 grad_loss: Optional[torch.Tensor] = None, chunk: int = 0, ws: Optional[torch.Tensor] = None):
+    """KL + hard-label CE mixture, backward: (dh [N,d] bf16, dW [V,d] fp32)."""
+    N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
+    _expect(label, "label", torch.int32, 1, dev)
+    _expect(lse, "lse", torch.float32, 1, dev)
+    _expect(lse1, "lse1", torch.float32, 1, dev)
+    if grad_loss is not None:
+        _expect(grad_loss.reshape(-1), "grad_loss", torch.float32, 1, dev)
+    if ws is None:
+        ws = alloc_workspace(N, d, V, K, chunk, dev)
+    dh = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    st = _lib.lib().fkl_mix_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), _ptr(label), N, d,
+                                     V, K, float(T), float(alpha), int(chunk), _ptr(lse), _ptr(lse1),
+                                     _ptr(grad_loss), _ptr(dh), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "fkl_mix_backward")
+    return dh, dW
+
+
 def forward_backward(h, W, idx, tlogit, mask, T: float, grad_loss: Optional[torch.Tensor] = None,
                      chunk: int = 0, ws: Optional[torch.Tensor] = None, loss: Optional[torch.Tensor] = None,
                      lse: Optional[torch.Tensor] = None, dh: Optional[torch.Tensor] = None,

@@ -124,28 +124,93 @@ __global__ void teacher_prep_kernel(const int32_t* __restrict__ idx, const float
     }
 }
 
-// lse_i and KL_i of one chunk from the per-tile partials (fixed tile order).
+// lse_i and KL_i of one chunk from the per-tile partials.  A block takes 32 rows;
+// 8 threads share a row, thread group g merging the tiles n = g, g + 8, ... (for a
+// fixed tile, 32 consecutive rows are one coalesced 128-byte read), and group 0
+// merges the 8 results in group order.  The order depends only on the tile index,
+// so a row's lse is the same whatever chunk it is in.
+constexpr int kFinRows = 32, kFinGroups = 8;
+
+__device__ __forceinline__ void merge_ml(float& M, float& L, float m, float l) {
+    if (l == 0.f) return;  // an empty part (no tile merged into it)
+    if (m > M) {
+        L = L * exp2f(M - m) + l;
+        M = m;
+    } else {
+        L += l * exp2f(m - M);
+    }
+}
+
 __global__ void fwd_finalize_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                                     const float* __restrict__ pg, int stride, int ntiles, int rows,
                                     const float* __restrict__ H, const uint8_t* __restrict__ valid,
                                     float T, float* __restrict__ lse, float* __restrict__ rowloss) {
+    __shared__ float s_m[kFinGroups][kFinRows], s_l[kFinGroups][kFinRows], s_g[kFinGroups][kFinRows];
+    const int rl = threadIdx.x % kFinRows, grp = threadIdx.x / kFinRows;
+    const int r = blockIdx.x * kFinRows + rl;
+    float M = -INFINITY, L = 0.f, G = 0.f;
+    if (r < rows) {
+        for (int n = grp; n < ntiles; n += kFinGroups) {
+            const size_t o = static_cast<size_t>(n) * stride + r;
+            G += pg[o];
+            merge_ml(M, L, pm[o], pl[o]);
+        }
+    }
+    s_m[grp][rl] = M;
+    s_l[grp][rl] = L;
+    s_g[grp][rl] = G;
+    __syncthreads();
+    if (grp != 0 || r >= rows) return;
+    for (int k = 1; k < kFinGroups; ++k) {
+        G += s_g[k][rl];
+        merge_ml(M, L, s_m[k][rl], s_l[k][rl]);
+    }
+    const float lse_r = (M + log2f(L)) * 0.69314718055994531f;
+    lse[r] = lse_r;
+    rowloss[r] = valid[r] ? (H[r] - G / T + lse_r) : 0.f;
+}
+
+// The same for the KL + hard-label cross-entropy mixture: also lse1_i (temperature
+// 1) and CE_i = lse1_i - z_{i,label_i}; rowloss_i = alpha KL_i + (1 - alpha) CE_i / T^2,
+// so that loss_reduce's T^2 / N_valid gives alpha T^2 KL + (1 - alpha) CE averaged
+// over the valid rows.  A valid row's label outside [0, V) records FKL_ERR_INDEX.
+__global__ void fwd_finalize_mix_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
+                                        const float* __restrict__ pg, const float* __restrict__ pm1,
+                                        const float* __restrict__ pl1, const float* __restrict__ pgy, int stride,
+                                        int ntiles, int rows, const float* __restrict__ H,
+                                        const uint8_t* __restrict__ valid, const int* __restrict__ label,
+                                        int64_t V, float T, float alpha, float* __restrict__ lse,
+                                        float* __restrict__ lse1, float* __restrict__ rowloss,
+                                        int* __restrict__ status) {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows) return;
-    float M = -INFINITY, L = 0.f, G = 0.f;
+    float M = -INFINITY, L = 0.f, G = 0.f, M1 = -INFINITY, L1 = 0.f, GY = 0.f;
     for (int n = 0; n < ntiles; ++n) {
         const size_t o = static_cast<size_t>(n) * stride + r;
-        const float m = pm[o], l = pl[o];
+        const float m = pm[o], l = pl[o], m1 = pm1[o], l1 = pl1[o];
         G += pg[o];
+        GY += pgy[o];
         if (m > M) {
             L = L * exp2f(M - m) + l;
             M = m;
         } else {
             L += l * exp2f(m - M);
         }
+        if (m1 > M1) {
+            L1 = L1 * exp2f(M1 - m1) + l1;
+            M1 = m1;
+        } else {
+            L1 += l1 * exp2f(m1 - M1);
+        }
     }
-    const float lse_r = (M + log2f(L)) * 0.69314718055994531f;
+    constexpr float kLn2 = 0.69314718055994531f;
+    const float lse_r = (M + log2f(L)) * kLn2;
+    const float lse1_r = (M1 + log2f(L1)) * kLn2;
     lse[r] = lse_r;
-    rowloss[r] = valid[r] ? (H[r] - G / T + lse_r) : 0.f;
+    lse1[r] = lse1_r;
+    const int y = label[r];
+    if (valid[r] && (y < 0 || static_cast<int64_t>(y) >= V)) atomicCAS(status, 0, static_cast<int>(FKL_ERR_INDEX));
+    rowloss[r] = valid[r] ? alpha * (H[r] - G / T + lse_r) + (1.f - alpha) * (lse1_r - GY) / (T * T) : 0.f;
 }
 
 // loss = T^2 * sum_i rowloss_i / N_valid, summed in fp64 in a fixed order by one block.
@@ -422,8 +487,18 @@ void launch_teacher_prep(const int32_t* idx, const float* tlogit, const uint8_t*
 void launch_fwd_finalize(const float* pm, const float* pl, const float* pg, int stride, int ntiles,
                          int rows, const float* H, const uint8_t* valid, float T, float* lse,
                          float* rowloss, cudaStream_t s) {
-    fwd_finalize_kernel<<<(rows + 127) / 128, 128, 0, s>>>(pm, pl, pg, stride, ntiles, rows, H, valid, T,
-                                                           lse, rowloss);
+    const int blocks = (rows + kFinRows - 1) / kFinRows;
+    fwd_finalize_kernel<<<blocks, kFinRows * kFinGroups, 0, s>>>(pm, pl, pg, stride, ntiles, rows, H, valid, T, lse,
+                                                                 rowloss);
+}
+
+void launch_fwd_finalize_mix(const float* pm, const float* pl, const float* pg, const float* pm1, const float* pl1,
+                             const float* pgy, int stride, int ntiles, int rows, const float* H,
+                             const uint8_t* valid, const int* label, int64_t V, float T, float alpha, float* lse,
+                             float* lse1, float* rowloss, int* status, cudaStream_t s) {
+    fwd_finalize_mix_kernel<<<(rows + 127) / 128, 128, 0, s>>>(pm, pl, pg, pm1, pl1, pgy, stride, ntiles, rows, H,
+                                                               valid, label, V, T, alpha, lse, lse1, rowloss,
+                                                               status);
 }
 
 void launch_loss_reduce(const float* rowloss, int64_t N, const int* n_valid, float T, float* loss,

@@ -268,6 +268,8 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
     // partials at once, so its partials share the dh partials' place.
     P.total = P.o_big + dz + std::max(part_fwd, part_dh);
     P.fwd_total = P.o_big + part_fwd;
+    // the KL + cross-entropy mixture's forward keeps six partial arrays, not three
+    P.total = std::max(P.total, P.o_big + 2 * part_fwd);
     return true;
 }
 
@@ -409,9 +411,17 @@ fkl_status grads_from_dz(const Plan& P, int64_t c, int rows, const CUtensorMap& 
 // The forward's launch sequence on a workspace of at least P.fwd_total bytes
 // (sizes and pointers already checked).  Only the 256-byte header needs to start
 // at zero; it is cleared here.  Every other region is written before it is read.
+// Extra inputs / outputs of the KL + hard-label cross-entropy mixture (null: plain KL).
+struct Mix {
+    const int32_t* label;  // [N] hard labels
+    float alpha;           // weight of the KL term
+    float* lse1;           // forward: [N] output, lse of z at temperature 1
+    const float* lse1_in;  // backward: the forward's lse1
+};
+
 fkl_status forward_enqueue(const Plan& P, const void* h, const void* W, const int32_t* idx,
                            const float* tlogit, const uint8_t* mask, float T, float* loss, float* lse,
-                           void* ws, cudaStream_t s) {
+                           void* ws, cudaStream_t s, const Mix* mix = nullptr) {
     const int64_t N = P.N, V = P.V;
     const int d = P.d, K = P.K;
     char* w = static_cast<char*>(ws);
@@ -426,6 +436,9 @@ fkl_status forward_enqueue(const Plan& P, const void* h, const void* W, const in
     float* pm = reinterpret_cast<float*>(w + P.o_big);
     float* pl = reinterpret_cast<float*>(w + P.o_big + pstride);
     float* pg = reinterpret_cast<float*>(w + P.o_big + 2 * pstride);
+    float* pm1 = reinterpret_cast<float*>(w + P.o_big + 3 * pstride);  // mixture only
+    float* pl1 = reinterpret_cast<float*>(w + P.o_big + 4 * pstride);
+    float* pgy = reinterpret_cast<float*>(w + P.o_big + 5 * pstride);
 
     FKL_CUDA_TRY(cudaMemsetAsync(w, 0, 256, s));
     const int sms = device_info().sms;
@@ -458,15 +471,102 @@ fkl_status forward_enqueue(const Plan& P, const void* h, const void* W, const in
         p.part_l = pl;
         p.part_g = pg;
         p.part_stride = P.Cc;
-        if (fkl_status st = run_gemm(KK_FWD_LSE, 256, 0, 0, EPI_LSE, tmH, tmW, tmW, p,
+        if (mix) {
+            p.T = T;  // the temperature-1 sum rescales z log2e / T by T
+            p.label = mix->label + row0;
+            p.part_m1 = pm1;
+            p.part_l1 = pl1;
+            p.part_gy = pgy;
+        }
+        if (fkl_status st = run_gemm(KK_FWD_LSE, 256, 0, 0, mix ? EPI_LSE_MIX : EPI_LSE, tmH, tmW, tmW, p,
                                      2.0 * rows * double(d) * double(V), s))
             return st;
-        FKL_SMALL(KK_FWD_FINALIZE,
-                  launch_fwd_finalize(pm, pl, pg, P.Cc, P.nt_v, rows, H, valid, T, lse + row0, rowloss + row0, s));
+        if (mix)
+            FKL_SMALL(KK_FWD_FINALIZE,
+                      launch_fwd_finalize_mix(pm, pl, pg, pm1, pl1, pgy, P.Cc, P.nt_v, rows, H, valid,
+                                              mix->label + row0, V, T, mix->alpha, lse + row0, mix->lse1 + row0,
+                                              rowloss + row0, status, s));
+        else
+            FKL_SMALL(KK_FWD_FINALIZE, launch_fwd_finalize(pm, pl, pg, P.Cc, P.nt_v, rows, H, valid, T, lse + row0,
+                                                           rowloss + row0, s));
     }
     FKL_SMALL(KK_LOSS_REDUCE, launch_loss_reduce(rowloss, N, n_valid, T, loss, s));
     return FKL_OK;
 }
+// The backward's launch sequence on a checked plan and workspace.
+fkl_status backward_enqueue(const Plan& P, const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                            const uint8_t* mask, float T, const float* lse, const float* grad_loss, void* dh,
+                            float* dW, void* ws, cudaStream_t s, const Mix* mix = nullptr) {
+    const int64_t N = P.N, V = P.V;
+    const int d = P.d, K = P.K;
+    char* w = static_cast<char*>(ws);
+    int* status = reinterpret_cast<int*>(w);
+    int* n_valid = status + 1;
+    int* sidx = reinterpret_cast<int*>(w + P.o_sidx);
+    float* sp = reinterpret_cast<float*>(w + P.o_sp);
+    float* H = reinterpret_cast<float*>(w + P.o_H);
+    uint8_t* valid = reinterpret_cast<uint8_t*>(w + P.o_valid);
+    void* dz = w + P.o_big;
+    float* part = reinterpret_cast<float*>(w + P.o_part_dh);
+
+    FKL_CUDA_TRY(cudaMemsetAsync(w, 0, 256, s));
+    const int sms = device_info().sms;
+    FKL_SMALL(KK_COUNT_VALID, launch_count_valid(tlogit, mask, N, K, n_valid, sms * 4, s));
+
+    CUtensorMap tmW_k, tmW_mn, tmDW;
+    FKL_TMAP(tmW_k, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, kVocabTile / 2);
+    FKL_TMAP(tmW_mn, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 64);
+    FKL_TMAP(tmDW, F32, dW, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32);
+    for (int64_t c = 0; c < P.n_chunks; ++c) {
+        const int64_t row0 = c * P.Cc;
+        const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
+        const double flop = 2.0 * rows * double(d) * double(V);
+        FKL_SMALL(KK_TEACHER_PREP,
+                  launch_teacher_prep(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status, s));
+        const char* hc = static_cast<const char*>(h) + size_t(row0) * d * 2;
+        CUtensorMap tmH_k, tmH_mn, tmDz_st, tmDz_k, tmDz_mn, tmPart;
+        FKL_TMAP(tmH_k, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 128);
+        FKL_TMAP(tmH_mn, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 64);
+        FKL_TMAP(tmDz_st, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 32);
+        FKL_TMAP(tmDz_k, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 128);
+        FKL_TMAP(tmDz_mn, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 64);
+        FKL_TMAP(tmPart, F32, part, uint64_t(d), uint64_t(P.splits) * P.Cc, uint64_t(d) * 4, 32, 32);
+
+        // dz = T g (q - s) / N_valid for this chunk's rows, bf16 [rows][V]
+        GemmParams p{};
+        p.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
+        p.n_tiles = P.nt_v;
+        p.splits = 1;
+        p.kb_total = static_cast<int>(cdiv(d, kBK));
+        p.m_fastest = 1;
+        p.M = rows;
+        p.Ncols = static_cast<int>(V);
+        p.status = status;
+        p.scale2 = kLog2e / T;
+        p.sidx = sidx;
+        p.sp = sp;
+        p.K = K;
+        p.lse = lse + row0;
+        p.valid = valid;
+        p.n_valid = n_valid;
+        p.grad = grad_loss;
+        p.T = T;
+        if (mix) {
+            p.label = mix->label + row0;
+            p.alpha = mix->alpha;
+            p.lse1 = mix->lse1_in + row0;
+        }
+        if (fkl_status st = run_gemm(KK_BWD_DZ, 256, 0, 0, mix ? EPI_DZ_MIX : EPI_DZ, tmH_k, tmW_k, tmDz_st, p,
+                                     flop, s))
+            return st;
+
+        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmH_mn, tmW_mn, tmPart, tmDW, part,
+                                          static_cast<char*>(dh) + size_t(row0) * d * 2, status, s))
+            return st;
+    }
+    return FKL_OK;
+}
+
 }  // namespace
 }  // namespace fkl
 
@@ -581,66 +681,46 @@ fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const 
     if (ws_bytes < P.total)
         return fail(FKL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, P.total);
     if (fkl_status st = device_ready()) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    char* w = static_cast<char*>(ws);
-    int* status = reinterpret_cast<int*>(w);
-    int* n_valid = status + 1;
-    int* sidx = reinterpret_cast<int*>(w + P.o_sidx);
-    float* sp = reinterpret_cast<float*>(w + P.o_sp);
-    float* H = reinterpret_cast<float*>(w + P.o_H);
-    uint8_t* valid = reinterpret_cast<uint8_t*>(w + P.o_valid);
-    void* dz = w + P.o_big;
-    float* part = reinterpret_cast<float*>(w + P.o_part_dh);
+    return backward_enqueue(P, h, W, idx, tlogit, mask, T, lse, grad_loss, dh, dW, ws,
+                            static_cast<cudaStream_t>(stream));
+}
 
-    FKL_CUDA_TRY(cudaMemsetAsync(w, 0, 256, s));
-    const int sms = device_info().sms;
-    FKL_SMALL(KK_COUNT_VALID, launch_count_valid(tlogit, mask, N, K, n_valid, sms * 4, s));
+fkl_status fkl_mix_forward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                           const uint8_t* mask, const int32_t* label, int64_t N, int d, int64_t V, int K, float T,
+                           float alpha, int chunk, float* loss, float* lse, float* lse1, void* ws, size_t ws_bytes,
+                           void* stream) {
+    g_err[0] = 0;
+    if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
+        return fail(FKL_ERR_INVALID_ARG, "%s", e);
+    if (!loss || !lse || !lse1 || !label) return fail(FKL_ERR_INVALID_ARG, "null loss, lse, lse1 or label pointer");
+    if (!(alpha >= 0.f && alpha <= 1.f)) return fail(FKL_ERR_INVALID_ARG, "alpha must be in [0, 1]");
+    Plan P;
+    make_plan(N, d, V, K, chunk, P);
+    if (ws_bytes < P.total)
+        return fail(FKL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, P.total);
+    if (fkl_status st = device_ready()) return st;
+    const Mix mix{label, alpha, lse1, nullptr};
+    return forward_enqueue(P, h, W, idx, tlogit, mask, T, loss, lse, ws, static_cast<cudaStream_t>(stream), &mix);
+}
 
-    CUtensorMap tmW_k, tmW_mn, tmDW;
-    FKL_TMAP(tmW_k, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, kVocabTile / 2);
-    FKL_TMAP(tmW_mn, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 64);
-    FKL_TMAP(tmDW, F32, dW, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32);
-    for (int64_t c = 0; c < P.n_chunks; ++c) {
-        const int64_t row0 = c * P.Cc;
-        const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
-        const double flop = 2.0 * rows * double(d) * double(V);
-        FKL_SMALL(KK_TEACHER_PREP,
-                  launch_teacher_prep(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status, s));
-        const char* hc = static_cast<const char*>(h) + size_t(row0) * d * 2;
-        CUtensorMap tmH_k, tmH_mn, tmDz_st, tmDz_k, tmDz_mn, tmPart;
-        FKL_TMAP(tmH_k, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 128);
-        FKL_TMAP(tmH_mn, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 64);
-        FKL_TMAP(tmDz_st, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 32);
-        FKL_TMAP(tmDz_k, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 128);
-        FKL_TMAP(tmDz_mn, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 64);
-        FKL_TMAP(tmPart, F32, part, uint64_t(d), uint64_t(P.splits) * P.Cc, uint64_t(d) * 4, 32, 32);
-
-        // dz = T g (q - s) / N_valid for this chunk's rows, bf16 [rows][V]
-        GemmParams p{};
-        p.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
-        p.n_tiles = P.nt_v;
-        p.splits = 1;
-        p.kb_total = static_cast<int>(cdiv(d, kBK));
-        p.m_fastest = 1;
-        p.M = rows;
-        p.Ncols = static_cast<int>(V);
-        p.status = status;
-        p.scale2 = kLog2e / T;
-        p.sidx = sidx;
-        p.sp = sp;
-        p.K = K;
-        p.lse = lse + row0;
-        p.valid = valid;
-        p.n_valid = n_valid;
-        p.grad = grad_loss;
-        p.T = T;
-        if (fkl_status st = run_gemm(KK_BWD_DZ, 256, 0, 0, EPI_DZ, tmH_k, tmW_k, tmDz_st, p, flop, s)) return st;
-
-        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmH_mn, tmW_mn, tmPart, tmDW, part,
-                                          static_cast<char*>(dh) + size_t(row0) * d * 2, status, s))
-            return st;
-    }
-    return FKL_OK;
+fkl_status fkl_mix_backward(const void* h, const void* W, const int32_t* idx, const float* tlogit,
+                            const uint8_t* mask, const int32_t* label, int64_t N, int d, int64_t V, int K, float T,
+                            float alpha, int chunk, const float* lse, const float* lse1, const float* grad_loss,
+                            void* dh, float* dW, void* ws, size_t ws_bytes, void* stream) {
+    g_err[0] = 0;
+    if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
+        return fail(FKL_ERR_INVALID_ARG, "%s", e);
+    if (!lse || !lse1 || !label || !dh || !dW) return fail(FKL_ERR_INVALID_ARG, "null lse, lse1, label, dh or dW");
+    if (!aligned16(dh) || !aligned16(dW)) return fail(FKL_ERR_INVALID_ARG, "dh and dW must be 16-byte aligned");
+    if (!(alpha >= 0.f && alpha <= 1.f)) return fail(FKL_ERR_INVALID_ARG, "alpha must be in [0, 1]");
+    Plan P;
+    make_plan(N, d, V, K, chunk, P);
+    if (ws_bytes < P.total)
+        return fail(FKL_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, P.total);
+    if (fkl_status st = device_ready()) return st;
+    const Mix mix{label, alpha, nullptr, lse1};
+    return backward_enqueue(P, h, W, idx, tlogit, mask, T, lse, grad_loss, dh, dW, ws,
+                            static_cast<cudaStream_t>(stream), &mix);
 }
 
 fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx, const float* tlogit,

@@ -39,11 +39,17 @@ enum KernelKind {
     KK_NUM
 };
 
-enum Epilogue { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_LSE_Y = 3, EPI_TMAX = 4, EPI_CAND = 5 };
+enum Epilogue {
+    EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_LSE_Y = 3, EPI_TMAX = 4, EPI_CAND = 5,
+    EPI_LSE_MIX = 6,  // EPI_LSE plus the hard-label terms of the KL + cross-entropy mixture
+    EPI_DZ_MIX = 7    // EPI_DZ of the mixture
+};
 
 // Epilogues that stage a tile in shared memory for a TMA store (the others write
 // a few values per row with plain stores).
-constexpr bool epi_staged(int epi) { return epi == EPI_DZ || epi == EPI_F32 || epi == EPI_LSE_Y; }
+constexpr bool epi_staged(int epi) {
+    return epi == EPI_DZ || epi == EPI_F32 || epi == EPI_LSE_Y || epi == EPI_DZ_MIX;
+}
 
 // Parameters of one persistent GEMM launch.  The unit space is
 // m_tiles (of 256 rows) x n_tiles (of BN columns) x splits; unit u maps to (m, n, s) with s slowest and either
@@ -79,6 +85,13 @@ struct GemmParams {
     int* cand_i;           // [M][cand_cap] their vocabulary ids
     int cand_cap;
     int* tie_i;            // [M][K] ids of the first K logits == theta
+    // EPI_LSE_MIX / EPI_DZ_MIX (KL + cross-entropy mixture)
+    const int* label;      // [M] hard label per row
+    float alpha;           // weight of the KL term
+    float* part_m1;        // EPI_LSE_MIX: [n_tiles][part_stride] running max of z log2e
+    float* part_l1;        //              sum of 2^(z log2e - max)
+    float* part_gy;        //              z at the label (0 in tiles without it)
+    const float* lse1;     // EPI_DZ_MIX: [M] natural-log lse of z (temperature 1)
 };
 
 // Launch helpers implemented in gemm_tc.cu.  Return cudaSuccess or the launch error.
@@ -98,6 +111,10 @@ void launch_teacher_prep(const int32_t* idx, const float* tlogit, const uint8_t*
 void launch_fwd_finalize(const float* pm, const float* pl, const float* pg, int stride, int ntiles,
                          int rows, const float* H, const uint8_t* valid, float T, float* lse,
                          float* rowloss, cudaStream_t s);
+void launch_fwd_finalize_mix(const float* pm, const float* pl, const float* pg, const float* pm1, const float* pl1,
+                             const float* pgy, int stride, int ntiles, int rows, const float* H,
+                             const uint8_t* valid, const int* label, int64_t V, float T, float alpha, float* lse,
+                             float* lse1, float* rowloss, int* status, cudaStream_t s);
 void launch_loss_reduce(const float* rowloss, int64_t N, const int* n_valid, float T, float* loss,
                         cudaStream_t s);
 void launch_dh_reduce(const float* part, int splits, size_t split_elems, int rows, int d, void* dh,

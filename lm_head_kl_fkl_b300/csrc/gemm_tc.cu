@@ -39,6 +39,9 @@
 //   EPI_DZ   the same logits recomputed: dz = coef * (2^(z log2e/T - lse log2e) - s)
 //            in bf16, staged per warp in swizzled shared memory and TMA-stored.
 //   EPI_F32  plain fp32 tile, TMA-stored or TMA reduce-added (dh partials, dW).
+//   EPI_LSE_MIX / EPI_DZ_MIX  the same for the KL + hard-label cross-entropy
+//            mixture: also a temperature-1 running max / sum and the logit at the
+//            row's label; dz gains (1 - alpha)/T (q_1 - onehot(label)) per row.
 //   EPI_TMAX each row's largest logit over the tile (teacher top-K, first pass).
 //   EPI_CAND every logit >= the row's threshold, appended to the row's candidate
 //            list with an atomic counter (teacher top-K, second pass); logits
@@ -159,7 +162,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr int NBUF = C::NBUF;
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "tile width");
     static_assert(NSUB == 1 || (NSUB == 2 && BN == 256 && EPI == EPI_F32), "wide tiles: 2 x 256, fp32 epilogue");
-    static_assert((EPI != EPI_DZ && EPI != EPI_LSE_Y) || BN % 64 == 0, "dz / logit boxes are 64 columns");
+    static_assert((EPI != EPI_DZ && EPI != EPI_DZ_MIX && EPI != EPI_LSE_Y) || BN % 64 == 0,
+                  "dz / logit boxes are 64 columns");
     static_assert(B_MN || BN / 2 <= 256, "K-major B box height");
 
     extern __shared__ uint8_t smem_raw[];
@@ -338,13 +342,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t tt = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                 static_cast<uint32_t>(acc * 256);
 
-            if constexpr (EPI == EPI_LSE) {
+            if constexpr (EPI == EPI_LSE || EPI == EPI_LSE_MIX) {
+                constexpr bool MIX = EPI == EPI_LSE_MIX;
                 const int v0 = n * BN;
                 TeacherCursor cur;
                 cur.seek(p.sidx, p.sp, row, row_ok, p.K, v0);
+                int ylab = -1;
+                if constexpr (MIX) ylab = row_ok ? __ldg(p.label + row) : -1;
                 if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
                 tc_fence_after();
                 float mrun = -INFINITY, lrun = 0.f, g = 0.f;
+                float m1run = -INFINITY, l1run = 0.f, gy = 0.f;  // temperature-1 terms (MIX only)
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     const int col0 = v0 + c * 32;
@@ -355,6 +363,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     while (cur.next_id < col0 + 32) {
                         g += cur.next_p * select32(z, cur.next_id - col0);
                         cur.advance();
+                    }
+                    if constexpr (MIX) {
+                        if (ylab >= col0 && ylab < col0 + 32) gy = select32(z, ylab - col0);
                     }
                     const int nv = p.Ncols - col0;
                     float cm0 = -INFINITY, cm1 = -INFINITY;
@@ -376,6 +387,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     lrun = lrun * ex2_approx(mrun - mnew) + ((s0 + s1) + (s2 + s3));
                     mrun = mnew;
+                    if constexpr (MIX) {  // the same online sum at temperature 1: z log2e = (z log2e / T) T
+                        float c1 = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) c1 = fmaxf(c1, z[j] * p.T);
+                        const float m1new = fmaxf(m1run, c1);
+                        float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            t0 += ex2_approx(z[j] * p.T - m1new);
+                            t1 += ex2_approx(z[j + 1] * p.T - m1new);
+                        }
+                        l1run = l1run * ex2_approx(m1run - m1new) + (t0 + t1);
+                        m1run = m1new;
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -385,6 +410,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     p.part_m[o] = mrun;
                     p.part_l[o] = lrun;
                     p.part_g[o] = g;
+                    if constexpr (MIX) {
+                        p.part_m1[o] = m1run;
+                        p.part_l1[o] = l1run;
+                        p.part_gy[o] = gy;
+                    }
                 }
             } else if constexpr (EPI == EPI_LSE_Y) {
                 const int v0 = n * BN;
@@ -523,16 +553,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
-            } else if constexpr (EPI == EPI_DZ) {
+            } else if constexpr (EPI == EPI_DZ || EPI == EPI_DZ_MIX) {
+                constexpr bool MIX = EPI == EPI_DZ_MIX;
                 const int v0 = n * BN;
                 TeacherCursor cur;
                 cur.seek(p.sidx, p.sp, row, row_ok, p.K, v0);
                 float lse2 = 0.f, coef = 0.f;
+                float lse1_2 = 0.f, cT = 0.f, c1 = 0.f;  // MIX: dz = cT (q_T - s) + c1 (q_1 - onehot)
+                int ylab = -1;
                 if (row_ok) {
                     lse2 = p.lse[row] * 1.4426950408889634f;
                     const int nvalid = *p.n_valid;
                     if (p.valid[row] && nvalid > 0)
                         coef = p.T * (p.grad ? *p.grad : 1.f) / static_cast<float>(nvalid);
+                    if constexpr (MIX) {
+                        lse1_2 = p.lse1[row] * 1.4426950408889634f;
+                        cT = coef * p.alpha;
+                        c1 = coef * (1.f - p.alpha) / p.T;
+                        ylab = __ldg(p.label + row);
+                    }
                 }
                 if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
                 tc_fence_after();
@@ -550,18 +589,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         __syncwarp();
                         tmem_ld32(tt + c2 * 64 + hh * 32, z);
                         const int nv = p.Ncols - cc;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            z[j] = (j < nv) ? ex2_approx(z[j] * p.scale2 - lse2) : 0.f;
-                        while (cur.next_id < cc + 32) {
-                            const int off = cur.next_id - cc;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) z[j] -= (j == off) ? cur.next_p : 0.f;
-                            cur.advance();
-                        }
                         uint32_t w[16];
+                        if constexpr (!MIX) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(coef * z[2 * j], coef * z[2 * j + 1]);
+                            for (int j = 0; j < 32; ++j)
+                                z[j] = (j < nv) ? ex2_approx(z[j] * p.scale2 - lse2) : 0.f;
+                            while (cur.next_id < cc + 32) {
+                                const int off = cur.next_id - cc;
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) z[j] -= (j == off) ? cur.next_p : 0.f;
+                                cur.advance();
+                            }
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(coef * z[2 * j], coef * z[2 * j + 1]);
+                        } else {
+                            constexpr float kL2e = 1.4426950408889634f;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                z[j] = (j < nv) ? cT * ex2_approx(z[j] * p.scale2 - lse2) +
+                                                      c1 * ex2_approx(z[j] * kL2e - lse1_2)
+                                                : 0.f;
+                            while (cur.next_id < cc + 32) {
+                                const int off = cur.next_id - cc;
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) z[j] -= (j == off) ? cT * cur.next_p : 0.f;
+                                cur.advance();
+                            }
+                            const int yoff = ylab - cc;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) z[j] -= (j == yoff) ? c1 : 0.f;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(z[2 * j], z[2 * j + 1]);
+                        }
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             st_shared_v4(buf + lane * 128u + ((static_cast<uint32_t>(hh * 4 + k) ^ (lane & 7u)) << 4),
@@ -659,6 +718,7 @@ size_t gemm_smem_bytes(int bn, int b_mn, int epi) {
     if (bn == BN_ * NS_ && b_mn == B_ && epi == E_) return PairCfg<BN_, NS_, B_, E_>::SMEM;
     FKL_SMEM_CASE(256, 1, 0, EPI_LSE) FKL_SMEM_CASE(256, 1, 0, EPI_DZ) FKL_SMEM_CASE(256, 1, 0, EPI_LSE_Y)
     FKL_SMEM_CASE(256, 1, 0, EPI_TMAX) FKL_SMEM_CASE(256, 1, 0, EPI_CAND)
+    FKL_SMEM_CASE(256, 1, 0, EPI_LSE_MIX) FKL_SMEM_CASE(256, 1, 0, EPI_DZ_MIX)
     FKL_SMEM_CASE(256, 2, 0, EPI_F32) FKL_SMEM_CASE(256, 2, 1, EPI_F32)
     FKL_SMEM_CASE(256, 1, 0, EPI_F32) FKL_SMEM_CASE(256, 1, 1, EPI_F32)
     FKL_SMEM_CASE(192, 1, 0, EPI_F32) FKL_SMEM_CASE(192, 1, 1, EPI_F32)
@@ -678,6 +738,16 @@ cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& 
     if (epi == EPI_DZ) {
         if (bn == 256 && a_mn == 0 && b_mn == 0)
             return launch_one<256, 1, 0, 0, EPI_DZ>(tmA, tmB, tmOut, p, max_pairs, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (epi == EPI_LSE_MIX) {
+        if (bn == 256 && a_mn == 0 && b_mn == 0)
+            return launch_one<256, 1, 0, 0, EPI_LSE_MIX>(tmA, tmB, tmOut, p, max_pairs, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (epi == EPI_DZ_MIX) {
+        if (bn == 256 && a_mn == 0 && b_mn == 0)
+            return launch_one<256, 1, 0, 0, EPI_DZ_MIX>(tmA, tmB, tmOut, p, max_pairs, stream);
         return cudaErrorInvalidValue;
     }
     if (epi == EPI_TMAX) {

@@ -39,6 +39,7 @@ import numpy as np
 __all__ = [
     "teacher_distribution", "row_valid", "student_lse", "forward", "backward",
     "rows_forward_backward", "dW_rows", "kl_rows_from_logits", "teacher_topk",
+    "forward_mix", "backward_mix",
 ]
 
 
@@ -228,3 +229,63 @@ def teacher_topk(h, W, K, rows=None, row_block=256):
         val[b0:b0 + len(rb)] = np.take_along_axis(z, order, axis=1)
         zs[b0:b0 + len(rb)] = z
     return idx, val, zs
+
+
+def forward_mix(h, W, idx, tlogit, mask, label, T, alpha, row_block=256):
+    """KL + hard-label cross-entropy: loss = alpha T^2 mean KL_i + (1 - alpha) mean CE_i.
+
+    "Distillyatsiya i szhatie modeley" (ml-book.com, section "Kak eto rabotaet:
+    myagkie metki i temperatura"): the student's loss mixes the KL between the
+    softened distributions with the ordinary cross-entropy on the true labels;
+    the weights (alpha, 1 - alpha) are the usual convex mix, the page's formula
+    being lost.  CE_i = lse1_i - z_{i,label_i} with lse1 the logsumexp of z at
+    temperature 1; both means run over the valid rows.  Returns the forward's
+    dict plus lse1 [N] and ce [N].
+    """
+    out = forward(h, W, idx, tlogit, mask, T, row_block)
+    h = np.asarray(h, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    label = np.asarray(label, dtype=np.int64)
+    N = h.shape[0]
+    lse1 = np.empty(N)
+    ce = np.empty(N)
+    for r0 in range(0, N, row_block):
+        r1 = min(N, r0 + row_block)
+        z = h[r0:r1] @ W.T
+        lse1[r0:r1] = _logsumexp_rows(z)
+        ce[r0:r1] = lse1[r0:r1] - z[np.arange(r1 - r0), label[r0:r1]]
+    valid, n_valid = out["valid"], out["n_valid"]
+    if n_valid > 0:
+        kl_mean = out["kl"][valid].sum() / n_valid
+        ce_mean = ce[valid].sum() / n_valid
+        out["loss"] = float(alpha) * float(T) ** 2 * kl_mean + (1.0 - float(alpha)) * ce_mean
+    out["lse1"] = lse1
+    out["ce"] = ce
+    return out
+
+
+def backward_mix(h, W, idx, tlogit, mask, label, T, alpha, grad_loss=1.0, row_block=256):
+    """dh, dW of forward_mix's loss times grad_loss:
+    dz_iv = g valid_i [alpha T (q_iv - s_iv) + (1 - alpha)(q1_iv - [v = label_i])] / N_valid."""
+    h = np.asarray(h, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    label = np.asarray(label, dtype=np.int64)
+    N = h.shape[0]
+    p, _ = teacher_distribution(tlogit, T)
+    valid = row_valid(mask, tlogit, T)
+    n_valid = int(valid.sum())
+    dh = np.zeros_like(h)
+    dW = np.zeros_like(W)
+    if n_valid == 0:
+        return dict(dh=dh, dW=dW, n_valid=0)
+    coef = valid.astype(np.float64) * float(grad_loss) / n_valid
+    for r0 in range(0, N, row_block):
+        r1 = min(N, r0 + row_block)
+        z = h[r0:r1] @ W.T
+        kl_part, _ = _dz_block(z, idx[r0:r1], p[r0:r1], T, coef[r0:r1] * float(T) * float(alpha))
+        q1 = np.exp(z - _logsumexp_rows(z)[:, None])
+        q1[np.arange(r1 - r0), label[r0:r1]] -= 1.0
+        dz = kl_part + (coef[r0:r1] * (1.0 - float(alpha)))[:, None] * q1
+        dh[r0:r1] = dz @ W
+        dW += dz.T @ h[r0:r1]
+    return dict(dh=dh, dW=dW, n_valid=n_valid)

@@ -286,9 +286,62 @@ def pin_topk_ties_and_permutation(orc):
         np.testing.assert_allclose(val_p[i], z[i, perm[idx_p[i]]], rtol=1e-14)
 
 
+# (M1) The KL + cross-entropy mixture against torch autograd through log_softmax,
+# kl_div and cross_entropy (library routines), for several alpha and T; alpha = 1
+# is the plain loss and alpha = 0 plain cross-entropy.
+def pin_mixture_autograd(orc):
+    if not hasattr(orc, "forward_mix"):
+        return  # only the numpy oracle carries the mixture
+    h, W, idx, t, mask, _ = _rand_problem(61, 48, 24, 211, 8, pad=3, overlap=True)
+    label = np.random.default_rng(62).integers(0, 211, 48)
+    for T, alpha in ((1.0, 0.5), (2.0, 0.3), (3.0, 1.0), (1.5, 0.0)):
+        out = orc.forward_mix(h, W, idx, t, mask, label, T, alpha)
+        g = orc.backward_mix(h, W, idx, t, mask, label, T, alpha, grad_loss=0.7)
+        ht = torch.tensor(h, dtype=torch.float64, requires_grad=True)
+        Wt = torch.tensor(W, dtype=torch.float64, requires_grad=True)
+        z = ht @ Wt.T
+        logq = torch.log_softmax(z / T, dim=1).gather(1, torch.tensor(idx, dtype=torch.long))
+        p = torch.softmax(torch.tensor(t, dtype=torch.float64) / T, dim=1)
+        keep = torch.tensor(mask != 0)
+        kl = F.kl_div(logq, p, reduction="none").sum(dim=1)[keep].mean()
+        ce = F.cross_entropy(z[keep], torch.tensor(label, dtype=torch.long)[keep])
+        loss = alpha * T * T * kl + (1 - alpha) * ce
+        (0.7 * loss).backward()
+        assert abs(out["loss"] - loss.item()) <= 1e-12 * abs(loss.item())
+        np.testing.assert_allclose(g["dh"], ht.grad.numpy(), rtol=1e-9, atol=1e-14)
+        np.testing.assert_allclose(g["dW"], Wt.grad.numpy(), rtol=1e-9, atol=1e-14)
+        if alpha == 1.0:
+            plain = orc.forward(h, W, idx, t, mask, T)
+            assert abs(plain["loss"] - out["loss"]) <= 1e-13 * abs(plain["loss"])
+
+
+# (M2) Mixture gradients against central finite differences of its loss.
+def pin_mixture_finite_differences(orc):
+    if not hasattr(orc, "forward_mix"):
+        return
+    h, W, idx, t, mask, _ = _rand_problem(67, 4, 3, 8, 3, pad=1, scale_w=0.8)
+    label = np.array([5, 0, 7, 2])
+    T, alpha, eps = 2.0, 0.4, 1e-6
+    g = orc.backward_mix(h, W, idx, t, mask, label, T, alpha)
+
+    def L(hh, WW):
+        return orc.forward_mix(hh, WW, idx, t, mask, label, T, alpha)["loss"]
+
+    for A, G, f in ((h, g["dh"], lambda a: L(a, W)), (W, g["dW"], lambda a: L(h, a))):
+        fd = np.zeros_like(A)
+        for i in range(A.shape[0]):
+            for j in range(A.shape[1]):
+                ap, am = A.copy(), A.copy()
+                ap[i, j] += eps
+                am[i, j] -= eps
+                fd[i, j] = (f(ap) - f(am)) / (2 * eps)
+        assert np.abs(G - fd).max() <= 1e-7 * max(1.0, np.abs(fd).max())
+
+
 ALL_PINS = [
     pin_kl_nonnegative, pin_zero_case, pin_chunk_invariance, pin_bias_shift,
     pin_finite_differences, pin_k1_cross_entropy, pin_autograd_general_k, pin_zero_sum,
     pin_uniform_student, pin_lse_library, pin_page_soft_labels, pin_degenerate_rows,
     pin_sampled_helpers, pin_topk_identity_head, pin_topk_ties_and_permutation,
+    pin_mixture_autograd, pin_mixture_finite_differences,
 ]

@@ -74,9 +74,15 @@ MUTATIONS = {
     "mean_over_all_rows": ("kl[valid].sum() / n_valid", "kl[valid].sum() / N"),
     "reverse_kl": ("kl = np.where(p > 0, p * (logp - logq), 0.0).sum(axis=1)",
                    "kl = np.where(p > 0, np.exp(logq) * (logq - logp), 0.0).sum(axis=1)"),
-    "dW_transposed_operand": ("dW += dz.T @ h[r0:r1]", "dW += (dz.T @ h[r0:r1])[::-1]"),
+    "dW_transposed_operand": ("coef[r0:r1])\n        dh[r0:r1] = dz @ W\n        dW += dz.T @ h[r0:r1]",
+                              "coef[r0:r1])\n        dh[r0:r1] = dz @ W\n        dW += (dz.T @ h[r0:r1])[::-1]"),
     "lse_missing_max_shift": ("return m + np.log(np.exp(a - m[:, None]).sum(axis=1))",
                               "return np.log(np.exp(a - m[:, None]).sum(axis=1))"),
+    "mixture_ce_without_lse": ("ce[r0:r1] = lse1[r0:r1] - z[np.arange(r1 - r0), label[r0:r1]]",
+                               "ce[r0:r1] = - z[np.arange(r1 - r0), label[r0:r1]]"),
+    "mixture_weights_swapped": ("(1.0 - float(alpha)) * ce_mean", "float(alpha) * ce_mean"),
+    "mixture_grad_label_sign": ("q1[np.arange(r1 - r0), label[r0:r1]] -= 1.0",
+                                "q1[np.arange(r1 - r0), label[r0:r1]] += 1.0"),
     "topk_ascending": ('order = np.argsort(-z, axis=1, kind="stable")[:, :K]',
                        'order = np.argsort(z, axis=1, kind="stable")[:, :K]'),
     "topk_ties_to_larger_id": ('order = np.argsort(-z, axis=1, kind="stable")[:, :K]',
