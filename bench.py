@@ -58,6 +58,32 @@ def kernel_digest():
     return m.hexdigest()[:12]
 
 
+def slowest_ms(ms, world, device):
+    """The slowest rank's time: each rank's number max-reduced (identity on one rank)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, steps, ms):
+    """Whole-job tokens/s: the tokens of every replica over the slowest rank's time."""
+    return tokens_per_rank * world * steps / (ms / 1e3)
+
+
+def per_kernel(prof, steps):
+    """{kernel: ms per step, TFLOP/s where the kernel does tensor work} from profile_read()."""
+    out = {}
+    for k, (ms, n, fl) in prof.items():
+        out[k] = {"ms_per_step": ms / steps, "launches": n}
+        if fl > 0:
+            out[k]["tflops"] = fl / (ms / 1e3) / 1e12
+    return out
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
@@ -266,15 +292,12 @@ def run_fused(args):
     launches = api.launch_count() - launches0
     ms = ev0.elapsed_time(ev1)
     prof = api.profile_read()
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = slowest_ms(ms, world, dev)
     peak_mem = torch.cuda.max_memory_allocated(dev)
     status = api.get_status(ws)
     ms_per_step = ms / args.steps
     tokens = N * world * args.steps
-    value = tokens / (ms / 1e3)
+    value = job_throughput(N, world, args.steps, ms)
     flop_step = 8.0 * N * d * V
     tflops = flop_step / (ms_per_step / 1e3) / 1e12
 
@@ -309,24 +332,24 @@ def run_fused(args):
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
+        api.profile_reset()
+        api.profile_enable(True)
         f0.record(stream)
         for _ in range(args.steps):
             step_fb()
         f1.record(stream)
         torch.cuda.synchronize()
-        fms = f0.elapsed_time(f1)
-        if world > 1:
-            tt = torch.tensor([fms], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            fms = float(tt.item())
+        api.profile_enable(False)
+        fb_kernels = per_kernel(api.profile_read(), args.steps)
+        fms = slowest_ms(f0.elapsed_time(f1), world, dev)
         fstep = fms / args.steps
         variants = {"forward_backward_one_call": {
-            "value": tokens / (fms / 1e3), "unit": "tokens/s", "ms_per_step": fstep,
+            "value": job_throughput(N, world, args.steps, fms), "unit": "tokens/s", "ms_per_step": fstep,
             "tflops_8NdV": flop_step / (fstep / 1e3) / 1e12,
             "tensor_tflops_6NdV": 0.75 * flop_step / (fstep / 1e3) / 1e12,
             "what": "fkl_forward_backward: each chunk's logits kept in fp16 between its loss and gradient "
                     "passes instead of recomputed (6 N d V tensor FLOP)",
-            "device_status": api.get_status(ws)}}
+            "kernels": fb_kernels, "device_status": api.get_status(ws)}}
 
         # the KL + hard-label cross-entropy mixture (alpha = 0.5) through its own entry points
         label = torch.from_numpy(np.random.default_rng(11).integers(0, V, N).astype(np.int32)).to(dev)
@@ -359,15 +382,19 @@ def run_fused(args):
             api.teacher_topk(h, W, K, ws=tk_ws)
         torch.cuda.synchronize()
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        api.profile_reset()
+        api.profile_enable(True)
         k0.record(stream)
         for _ in range(args.steps):
             api.teacher_topk(h, W, K, ws=tk_ws)
         k1.record(stream)
         torch.cuda.synchronize()
+        api.profile_enable(False)
+        tk_kernels = per_kernel(api.profile_read(), args.steps)
         kstep = k0.elapsed_time(k1) / args.steps
         topk = {"value": N / (kstep / 1e3), "unit": "tokens/s", "ms_per_step": kstep,
                 "tflops_4NdV": 4.0 * N * d * V / (kstep / 1e3) / 1e12, "K": K,
-                "workspace_gb": tk_ws.numel() / 1e9,
+                "workspace_gb": tk_ws.numel() / 1e9, "kernels": tk_kernels,
                 "what": "fkl_teacher_topk: two tensor-core passes over z = h W^T (per-tile max, then the "
                         "logits above the K-th largest tile max), top-K selection per row",
                 "device_status": api.get_status(tk_ws)}
@@ -402,13 +429,9 @@ def run_fused(args):
             stream.synchronize()  # the loss is read on the host every step
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([ems], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
+        ems = slowest_ms(e0.elapsed_time(e1), world, dev)
         bi = sum(a.numel() * a.element_size() for a in (hp, ip, tp, mp))
-        e2e = {"value": tokens / (ems / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+        e2e = {"value": job_throughput(N, world, args.steps, ems), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": 4, "ms_per_step": ems / args.steps,
                "resident": "W (model weight) stays on the device; h, teacher ids/logits and mask are copied per step"}
 
