@@ -201,6 +201,54 @@ def config_dict(c, chunk, world):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
+def memory_stress(api, dev, stream, chunk, steps):
+    """Forward + backward of the gpt-oss-120b-like memory-stress workload (N = 131072,
+    d = 2880, V = 201088, K = 100): time per step and peak device memory, against
+    what the inputs and the gradients alone occupy."""
+    import torch
+    from lm_head_kl_fkl_b300 import synth
+    c = synth.CONFIGS[4]
+    x = synth.config_inputs(4)
+    N, d, V, K, T = c.N, c.d, c.V, c.K, c.T
+    torch.cuda.reset_peak_memory_stats(dev)
+    base0 = torch.cuda.memory_allocated(dev)
+    h = torch.from_numpy(x["h"].view(np.int16)).view(torch.bfloat16).to(dev)
+    W = torch.from_numpy(x["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    idx, t, mask = (torch.from_numpy(x[k]).to(dev) for k in ("idx", "t", "mask"))
+    del x
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dh = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    io = torch.cuda.memory_allocated(dev) - base0
+    ws = api.alloc_workspace(N, d, V, K, chunk, dev)
+
+    def step():
+        api.forward(h, W, idx, t, mask, T, chunk, ws=ws, loss=loss, lse=lse)
+        api.backward(h, W, idx, t, mask, T, lse, chunk=chunk, ws=ws, dh=dh, dW=dW)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    peak = torch.cuda.max_memory_allocated(dev) - base0
+    status = api.get_status(ws)
+    out = {"workload": f"{c.name} fused top-K KL loss", "N": N, "d": d, "V": V, "K": K, "steps": steps,
+           "ms_per_step": ms, "value": N / (ms / 1e3), "unit": "tokens/s",
+           "tflops": 8.0 * N * d * V / (ms / 1e3) / 1e12,
+           "peak_mem_gb": peak / 1e9, "inputs_and_grads_gb": io / 1e9, "workspace_gb": ws.numel() / 1e9,
+           "peak_beyond_inputs_and_grads_gb": (peak - io) / 1e9, "device_status": status}
+    del h, W, idx, t, mask, loss, lse, dh, dW, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -439,6 +487,17 @@ def run_fused(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x)
 
+    # ---- the memory-stress workload (N = 131072): peak device memory of the same call pair
+    mem = None
+    ws_gb = ws.numel() / 1e9
+    if not args.no_memory_stress and args.config == 3 and args.shape is None:
+        del h, W, idx, t, mask, ws, loss, lse, dh, dW
+        if not args.no_e2e:
+            del h_in, idx_in, t_in, m_in
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        mem = memory_stress(api, dev, stream, args.chunk, min(args.steps, 3))
+
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -449,10 +508,10 @@ def run_fused(args):
                                       "sustained": tflops / peaks["bf16_tflops_sustained"],
                                       "kind": peaks_kind},
                 "peak_mem_gb": peak_mem / 1e9,
-                "workspace_gb": ws.numel() / 1e9,
+                "workspace_gb": ws_gb,
                 "resident_gb": base_mem / 1e9,
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-                "variants": variants, "teacher_topk": topk,
+                "variants": variants, "teacher_topk": topk, "memory_stress": mem,
                 "clocks": clk.summary(), "gpu_launches": launches, "device_status": status,
                 "kernel_digest": kernel_digest()}
         print(json.dumps(line), flush=True)
@@ -473,6 +532,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the one-call forward+backward timing")
+    ap.add_argument("--no-memory-stress", action="store_true", help="skip the N=131072 peak-memory leg")
     ap.add_argument("--shape", type=lambda s: tuple(int(v) for v in s.split(",")), default=None,
                     help="N,d,V,K: a smaller case of the chosen workload (profiling captures)")
     args = ap.parse_args()

@@ -124,12 +124,12 @@ __global__ void teacher_prep_kernel(const int32_t* __restrict__ idx, const float
     }
 }
 
-// lse_i and KL_i of one chunk from the per-tile partials.  A block takes 32 rows;
-// 8 threads share a row, thread group g merging the tiles n = g, g + 8, ... (for a
-// fixed tile, 32 consecutive rows are one coalesced 128-byte read), and group 0
-// merges the 8 results in group order.  The order depends only on the tile index,
-// so a row's lse is the same whatever chunk it is in.
-constexpr int kFinRows = 32, kFinGroups = 8;
+// lse_i and KL_i of one chunk from the per-tile partials.  A block takes 8 rows;
+// 32 threads share a row, thread group g merging the tiles n = g, g + 32, ... (for
+// a fixed tile, the 8 rows are one 32-byte sector), and group 0 merges the 32
+// results in group order.  The order depends only on the tile index, so a row's
+// lse is the same whatever chunk it is in.
+constexpr int kFinRows = 8, kFinGroups = 32;
 
 __device__ __forceinline__ void merge_ml(float& M, float& L, float m, float l) {
     if (l == 0.f) return;  // an empty part (no tile merged into it)
@@ -182,26 +182,32 @@ __global__ void fwd_finalize_mix_kernel(const float* __restrict__ pm, const floa
                                         int64_t V, float T, float alpha, float* __restrict__ lse,
                                         float* __restrict__ lse1, float* __restrict__ rowloss,
                                         int* __restrict__ status) {
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= rows) return;
+    __shared__ float s_v[6][kFinGroups][kFinRows];
+    const int rl = threadIdx.x % kFinRows, grp = threadIdx.x / kFinRows;
+    const int r = blockIdx.x * kFinRows + rl;
     float M = -INFINITY, L = 0.f, G = 0.f, M1 = -INFINITY, L1 = 0.f, GY = 0.f;
-    for (int n = 0; n < ntiles; ++n) {
-        const size_t o = static_cast<size_t>(n) * stride + r;
-        const float m = pm[o], l = pl[o], m1 = pm1[o], l1 = pl1[o];
-        G += pg[o];
-        GY += pgy[o];
-        if (m > M) {
-            L = L * exp2f(M - m) + l;
-            M = m;
-        } else {
-            L += l * exp2f(m - M);
+    if (r < rows) {
+        for (int n = grp; n < ntiles; n += kFinGroups) {
+            const size_t o = static_cast<size_t>(n) * stride + r;
+            G += pg[o];
+            GY += pgy[o];
+            merge_ml(M, L, pm[o], pl[o]);
+            merge_ml(M1, L1, pm1[o], pl1[o]);
         }
-        if (m1 > M1) {
-            L1 = L1 * exp2f(M1 - m1) + l1;
-            M1 = m1;
-        } else {
-            L1 += l1 * exp2f(m1 - M1);
-        }
+    }
+    s_v[0][grp][rl] = M;
+    s_v[1][grp][rl] = L;
+    s_v[2][grp][rl] = G;
+    s_v[3][grp][rl] = M1;
+    s_v[4][grp][rl] = L1;
+    s_v[5][grp][rl] = GY;
+    __syncthreads();
+    if (grp != 0 || r >= rows) return;
+    for (int k = 1; k < kFinGroups; ++k) {
+        G += s_v[2][k][rl];
+        GY += s_v[5][k][rl];
+        merge_ml(M, L, s_v[0][k][rl], s_v[1][k][rl]);
+        merge_ml(M1, L1, s_v[3][k][rl], s_v[4][k][rl]);
     }
     constexpr float kLn2 = 0.69314718055994531f;
     const float lse_r = (M + log2f(L)) * kLn2;
@@ -333,11 +339,23 @@ __global__ void topk_threshold_kernel(const float* __restrict__ part_m, int stri
     if (r >= rows) return;
     float th = -INFINITY;
     if (ntiles >= K) {
+        // the row's tile maxima, lane-strided, in registers (up to 32 x kTh of them),
+        // the rest re-read from memory on each step of the search
+        constexpr int kTh = 32;
+        uint32_t key[kTh];
+#pragma unroll
+        for (int j = 0; j < kTh; ++j) {
+            const int n = lane + 32 * j;
+            key[j] = n < ntiles ? fkey(part_m[static_cast<size_t>(n) * stride + r]) : 0u;
+        }
         uint32_t t = 0;  // largest key with at least K tile maxima at or above it
         for (int b = 31; b >= 0; --b) {
             const uint32_t cand = t | (1u << b);
             int c = 0;
-            for (int n = lane; n < ntiles; n += 32) c += fkey(part_m[static_cast<size_t>(n) * stride + r]) >= cand;
+#pragma unroll
+            for (int j = 0; j < kTh; ++j) c += key[j] >= cand;
+            for (int n = lane + 32 * kTh; n < ntiles; n += 32)
+                c += fkey(part_m[static_cast<size_t>(n) * stride + r]) >= cand;
             for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
             if (c >= K) t = cand;
         }
@@ -496,9 +514,10 @@ void launch_fwd_finalize_mix(const float* pm, const float* pl, const float* pg, 
                              const float* pgy, int stride, int ntiles, int rows, const float* H,
                              const uint8_t* valid, const int* label, int64_t V, float T, float alpha, float* lse,
                              float* lse1, float* rowloss, int* status, cudaStream_t s) {
-    fwd_finalize_mix_kernel<<<(rows + 127) / 128, 128, 0, s>>>(pm, pl, pg, pm1, pl1, pgy, stride, ntiles, rows, H,
-                                                               valid, label, V, T, alpha, lse, lse1, rowloss,
-                                                               status);
+    const int blocks = (rows + kFinRows - 1) / kFinRows;
+    fwd_finalize_mix_kernel<<<blocks, kFinRows * kFinGroups, 0, s>>>(pm, pl, pg, pm1, pl1, pgy, stride, ntiles, rows,
+                                                                     H, valid, label, V, T, alpha, lse, lse1, rowloss,
+                                                                     status);
 }
 
 void launch_loss_reduce(const float* rowloss, int64_t N, const int* n_valid, float T, float* loss,

@@ -119,11 +119,27 @@ DeviceInfo query_device() {
     return di;
 }
 
+// Facts of the current device, queried once per device ordinal.
 const DeviceInfo& device_info() {
-    static std::once_flag once;
-    static DeviceInfo di;
-    std::call_once(once, [] { di = query_device(); });
-    return di;
+    constexpr int kMaxDevices = 256;
+    static std::mutex mu;
+    static DeviceInfo infos[kMaxDevices];
+    static bool have[kMaxDevices] = {};
+    static DeviceInfo none;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        std::lock_guard<std::mutex> lock(mu);
+        none = DeviceInfo{};
+        snprintf(none.why, sizeof(none.why), "no usable CUDA device");
+        return none;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        infos[dev] = query_device();
+        have[dev] = true;
+    }
+    return infos[dev];
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
