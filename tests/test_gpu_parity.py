@@ -163,3 +163,22 @@ def test_row_shards_combine_to_full_batch():
     assert rel_l2(np.concatenate(dh), full["dh"]) <= 1e-3
     assert rel_l2(dW, full["dW"]) <= 1e-4
     _check(x, dict(loss=loss, lse=np.concatenate(lse), dh=np.concatenate(dh), dW=dW))
+
+
+EDGE = [
+    # N, d, V, K, T, index, chunk: the smallest hidden size, one partial vocabulary tile,
+    # K = V, the largest K, extreme temperatures
+    (200, 8, 777, 5, 1.0, "uniform", 0),
+    (150, 64, 8, 3, 1.0, "uniform", 0),
+    (130, 64, 40, 40, 1.0, "uniform", 0),
+    (260, 96, 3000, 256, 1.0, "uniform", 128),
+    (300, 128, 2000, 20, 0.05, "uniform", 128),
+    (300, 128, 2000, 20, 20.0, "half-student", 0),
+]
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "N{}_d{}_V{}_K{}_T{}".format(*s[:5]))
+def test_edge_sizes(shape):
+    N, d, V, K, T, index, chunk = shape
+    x = synth.make_inputs(N, d, V, K, T, 0.05, index, seed=9200 + N + V)
+    _check(x, run_fused(to_device(x), chunk=chunk))
