@@ -230,6 +230,16 @@ int64_t fkl_launch_count(void);
 fkl_status fkl_selftest_gemm(const void* A, const void* B, float* C, int M, int N, int K,
                              int a_mn, int b_mn, int bn, void* ws, void* stream);
 
+/* ---- bounded-wait self-test (not part of the loss) -------------------------
+ * Every pipeline wait of the kernels gives up after a time limit, records
+ * FKL_ERR_TIMEOUT in the status word and lets the kernel return, so that a
+ * defect ends in an error instead of a hung GPU.  This entry runs that same wait
+ * in a one-thread kernel on a barrier nothing ever arrives on, with limit_ns
+ * (1e3 .. 2e9) instead of the pipelines' 2 s: afterwards fkl_get_status(ws)
+ * reports FKL_ERR_TIMEOUT and the context stays usable.  `ws`: >= 256 bytes of
+ * device memory; its status word is cleared first. */
+fkl_status fkl_selftest_wait_timeout(void* ws, int64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

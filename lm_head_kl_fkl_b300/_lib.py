@@ -51,6 +51,7 @@ SIGNATURES = {
                                  ctypes.POINTER(c_double), c_int]),
     "fkl_kernel_name": (c_char_p, [c_int]),
     "fkl_launch_count": (c_i64, []),
+    "fkl_selftest_wait_timeout": (c_int, [c_void_p, c_i64, c_void_p]),
     "fkl_selftest_gemm": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                   c_int, c_void_p, c_void_p]),
 }

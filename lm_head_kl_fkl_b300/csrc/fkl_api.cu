@@ -88,7 +88,7 @@ const char* const kKindNames[KK_NUM] = {
     "count_valid", "teacher_prep", "fwd_gemm_lse", "fwd_finalize", "loss_reduce",
     "bwd_gemm_dz", "bwd_gemm_dh", "dh_reduce", "bwd_gemm_dw", "selftest_gemm",
     "fb_gemm_lse_keep", "fb_dz_from_logits",
-    "tk_gemm_tile_max", "tk_threshold", "tk_gemm_candidates", "tk_select",
+    "tk_gemm_tile_max", "tk_threshold", "tk_gemm_candidates", "tk_select", "selftest_wait",
 };
 
 // ---------------------------------------------------------------- device facts
@@ -932,6 +932,22 @@ int fkl_profile_read(double* ms, int64_t* launches, double* flop, int n) {
 const char* fkl_kernel_name(int kind) { return (kind >= 0 && kind < KK_NUM) ? kKindNames[kind] : ""; }
 
 int64_t fkl_launch_count(void) { return g_launches.load(); }
+
+fkl_status fkl_selftest_wait_timeout(void* ws, int64_t limit_ns, void* stream) {
+    g_err[0] = 0;
+    if (!ws || !aligned16(ws)) return fail(FKL_ERR_INVALID_ARG, "ws must be a 16-byte aligned device pointer");
+    if (limit_ns < 1000 || limit_ns > 2000000000) return fail(FKL_ERR_INVALID_ARG, "limit_ns must be in [1e3, 2e9]");
+    if (fkl_status st = device_ready()) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FKL_CUDA_TRY(cudaMemsetAsync(ws, 0, 256, s));
+    cudaError_t e;
+    {
+        LaunchScope ls(KK_SELFTEST_WAIT, 0.0, s);
+        e = launch_wait_timeout(static_cast<int*>(ws), static_cast<uint64_t>(limit_ns), s);
+    }
+    if (e != cudaSuccess) return fail(FKL_ERR_CUDA, "selftest_wait launch: %s", cudaGetErrorString(e));
+    return FKL_OK;
+}
 
 fkl_status fkl_selftest_gemm(const void* A, const void* B, float* C, int M, int N, int K, int a_mn, int b_mn,
                              int bn, void* ws, void* stream) {

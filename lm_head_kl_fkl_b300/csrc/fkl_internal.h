@@ -36,6 +36,7 @@ enum KernelKind {
     KK_TK_THRESHOLD,   // teacher top-K: per-row K-th largest tile max
     KK_TK_GEMM_CAND,   // teacher top-K: tcgen05 GEMM again, logits >= threshold appended per row
     KK_TK_SELECT,      // teacher top-K: per-row selection and sort of the candidates
+    KK_SELFTEST_WAIT,  // bounded-wait self-test
     KK_NUM
 };
 
@@ -101,6 +102,7 @@ cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& 
                         const CUtensorMap& tmB, const CUtensorMap& tmOut, const GemmParams& p,
                         int max_pairs, cudaStream_t stream);
 size_t gemm_smem_bytes(int bn, int b_mn, int epi);
+cudaError_t launch_wait_timeout(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 // Small kernels implemented in aux_kernels.cu.
 void launch_count_valid(const float* tlogit, const uint8_t* mask, int64_t N, int K, int* n_valid,

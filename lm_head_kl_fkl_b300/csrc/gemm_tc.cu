@@ -57,6 +57,7 @@
 // MN-major tiles as boxes {64 (MN), 64 (K)} side by side, 8 KB apart.
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "ptx.cuh"
 
@@ -683,32 +684,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- bounded-wait self-test
+// One thread waits on an mbarrier that nothing arrives on, with the pipeline's
+// bounded wait and a short limit: the wait gives up, records FKL_ERR_TIMEOUT in
+// the status word and the kernel returns (no copy or MMA is in flight).
+__global__ void wait_timeout_kernel(int* status, uint64_t limit_ns) {
+    __shared__ alignas(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    mbar_wait_for(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+}
+
+cudaError_t launch_wait_timeout(int* status, uint64_t limit_ns, cudaStream_t stream) {
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- host dispatch
 template <int BN, int NSUB, int A_MN, int B_MN, int EPI>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmOut,
                               const GemmParams& p, int max_pairs, cudaStream_t stream) {
     constexpr size_t smem = PairCfg<BN, NSUB, B_MN, EPI>::SMEM;
     static_assert(smem <= 232448, "shared memory per CTA");
-    static int pairs_resident = 0;
-    if (pairs_resident == 0) {
-        auto kern = gemm_kernel<BN, NSUB, A_MN, B_MN, EPI>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * max_pairs);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = smem;
-        int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-        if (e != cudaSuccess || clusters <= 0) {
-            cudaGetLastError();
-            clusters = max_pairs;
+    // Per device: the shared-memory attribute is set and the resident pair count
+    // queried on the first launch of this instantiation there.
+    constexpr int kMaxDevices = 256;
+    static std::mutex mu;
+    static int pairs_resident[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int resident;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (pairs_resident[dev] == 0) {
+            auto kern = gemm_kernel<BN, NSUB, A_MN, B_MN, EPI>;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * max_pairs);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = smem;
+            int clusters = 0;
+            e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+            if (e != cudaSuccess || clusters <= 0) {
+                cudaGetLastError();
+                clusters = max_pairs;
+            }
+            pairs_resident[dev] = clusters < max_pairs ? clusters : max_pairs;
         }
-        pairs_resident = clusters < max_pairs ? clusters : max_pairs;
+        resident = pairs_resident[dev];
     }
     const long long units = static_cast<long long>(p.m_tiles) * p.n_tiles * p.splits;
-    const int pairs = static_cast<int>(units < pairs_resident ? units : pairs_resident);
+    const int pairs = static_cast<int>(units < resident ? units : resident);
     gemm_kernel<BN, NSUB, A_MN, B_MN, EPI><<<2 * pairs, kThreads, smem, stream>>>(tmA, tmB, tmOut, p);
     return cudaGetLastError();
 }

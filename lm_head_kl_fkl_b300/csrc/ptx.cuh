@@ -56,23 +56,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of parity `parity` to complete.  Returns false (and
-// raises the CTA's abort flag and the device status) after kWaitLimitNs, or
-// at once if another role of the CTA has already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+// raises the CTA's abort flag and the device status) after limit_ns, or at
+// once if another role of the CTA has already aborted.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              int* status, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 15u) == 0) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 set_status(status, FKL_ERR_TIMEOUT);
                 return false;
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+    return mbar_wait_for(bar, parity, abort_flag, status, kWaitLimitNs);
 }
 
 // Time-bounded wait that ignores the abort flag (used while draining after an abort).

@@ -40,6 +40,8 @@ _SIGS = {
     "fklo_dW_rows": [_d, _d, _i32, _d, _u8, _L, _L, _L, _L, _F, _F, _d, _i64p, _L, _I, _d],
     "fklo_student_lse": [_d, _d, _L, _L, _L, _F, _I, _d],
     "fklo_teacher_topk": [_d, _d, _L, _L, _L, _L, _I, _i64p, _d],
+    "fklo_forward_mix": [_d, _d, _i32, _d, _u8, _i32, _L, _L, _L, _L, _F, _F, _I, _d, _d, _d, _d, _u8, _d, _i64p],
+    "fklo_backward_mix": [_d, _d, _i32, _d, _u8, _i32, _L, _L, _L, _L, _F, _F, _F, _I, _d, _d],
 }
 
 
@@ -173,6 +175,42 @@ def _teacher_topk(self, h, W, K, rows=None, row_block=256):
 
 
 CppOracle.teacher_topk = _teacher_topk
+
+
+def _forward_mix(self, h, W, idx, tlogit, mask, label, T, alpha, row_block=256):
+    """KL + hard-label cross-entropy mixture: the forward's dict plus lse1 and ce."""
+    del row_block
+    h, W, idx, t, m = self._common(h, W, idx, tlogit, mask)
+    lab = np.ascontiguousarray(np.asarray(label, dtype=np.int32))
+    N, d = h.shape
+    V, K = W.shape[0], idx.shape[1]
+    lse, lse1, kl, ce = (np.empty(N) for _ in range(4))
+    valid = np.empty(N, dtype=np.uint8)
+    loss = ctypes.c_double()
+    nv = ctypes.c_int64()
+    self.lib.fklo_forward_mix(_p(h, _d), _p(W, _d), _p(idx, _i32), _p(t, _d), None if m is None else _p(m, _u8),
+                              _p(lab, _i32), N, d, V, K, float(T), float(alpha), threads(), _p(lse, _d),
+                              _p(lse1, _d), _p(kl, _d), _p(ce, _d), _p(valid, _u8), ctypes.byref(loss),
+                              ctypes.byref(nv))
+    return dict(loss=loss.value, lse=lse, lse1=lse1, kl=kl, ce=ce, n_valid=int(nv.value), valid=valid.astype(bool))
+
+
+def _backward_mix(self, h, W, idx, tlogit, mask, label, T, alpha, grad_loss=1.0, row_block=256):
+    """dh, dW of the mixture times grad_loss."""
+    del row_block
+    h, W, idx, t, m = self._common(h, W, idx, tlogit, mask)
+    lab = np.ascontiguousarray(np.asarray(label, dtype=np.int32))
+    N, d = h.shape
+    V, K = W.shape[0], idx.shape[1]
+    dh, dW = np.empty((N, d)), np.empty((V, d))
+    self.lib.fklo_backward_mix(_p(h, _d), _p(W, _d), _p(idx, _i32), _p(t, _d), None if m is None else _p(m, _u8),
+                               _p(lab, _i32), N, d, V, K, float(T), float(alpha), float(grad_loss), threads(),
+                               _p(dh, _d), _p(dW, _d))
+    return dict(dh=dh, dW=dW)
+
+
+CppOracle.forward_mix = _forward_mix
+CppOracle.backward_mix = _backward_mix
 
 
 def load() -> CppOracle:

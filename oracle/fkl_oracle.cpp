@@ -119,6 +119,20 @@ void dz_row(const double* z, const int32_t* idx, const double* p, int64_t V, int
     for (int64_t v = 0; v < V; ++v) dz[v] *= coef;
 }
 
+// The forward of one row: its full logit row z, lse (at T) and KL.
+void forward_row(const double* hi, const double* W, const int32_t* idx_i, const double* p, int64_t d, int64_t V,
+                 int64_t K, double T, double* z, double* lse, double* kl) {
+    logit_row(hi, W, d, V, z);
+    *lse = lse_row(z, V, T);
+    *kl = kl_row(z, idx_i, p, K, T, *lse);
+}
+
+// dh_i += sum_v dz_iv W_v.
+void add_dh_row(const double* dzr, const double* W, int64_t V, int64_t d, double* dhi) {
+    for (int64_t v = 0; v < V; ++v)
+        for (int64_t j = 0; j < d; ++j) dhi[j] += dzr[v] * W[v * d + j];
+}
+
 int64_t count_valid(const double* t, const uint8_t* mask, int64_t N, int64_t K, double T) {
     std::vector<double> p(static_cast<size_t>(K));
     int64_t n = 0;
@@ -144,9 +158,7 @@ void fklo_forward(const double* h, const double* W, const int32_t* idx, const do
         for (int64_t i = b; i < e; ++i) {
             const bool has = teacher_row(t + i * K, K, T, p.data());
             valid[i] = row_valid(mask, i, has) ? 1 : 0;
-            logit_row(h + i * d, W, d, V, z.data());
-            lse[i] = lse_row(z.data(), V, T);
-            kl[i] = kl_row(z.data(), idx + i * K, p.data(), K, T, lse[i]);
+            forward_row(h + i * d, W, idx + i * K, p.data(), d, V, K, T, z.data(), lse + i, kl + i);
         }
     });
     int64_t nv = 0;
@@ -184,9 +196,7 @@ void fklo_backward(const double* h, const double* W, const int32_t* idx, const d
                 double* dzr = dz.data() + r * V;
                 logit_row(h + i * d, W, d, V, z.data());
                 dz_row(z.data(), idx + i * K, p.data(), V, K, T, lse_row(z.data(), V, T), coef, dzr);
-                double* dhi = dh + i * d;
-                for (int64_t v = 0; v < V; ++v)
-                    for (int64_t j = 0; j < d; ++j) dhi[j] += dzr[v] * W[v * d + j];
+                add_dh_row(dzr, W, V, d, dh + i * d);
             }
         });
         parallel_for(V, threads, [&](int64_t b, int64_t e) {
@@ -213,16 +223,13 @@ void fklo_rows(const double* h, const double* W, const int32_t* idx, const doubl
         for (int64_t r = b; r < e; ++r) {
             const int64_t i = rows[r];
             const bool has = teacher_row(t + i * K, K, T, p.data());
-            logit_row(h + i * d, W, d, V, z.data());
-            lse[r] = lse_row(z.data(), V, T);
-            kl[r] = kl_row(z.data(), idx + i * K, p.data(), K, T, lse[r]);
+            forward_row(h + i * d, W, idx + i * K, p.data(), d, V, K, T, z.data(), lse + r, kl + r);
             double* dhr = dh + r * d;
             std::fill(dhr, dhr + d, 0.0);
             if (nv == 0) continue;
             const double coef = row_valid(mask, i, has) ? grad_loss * T / static_cast<double>(nv) : 0.0;
             dz_row(z.data(), idx + i * K, p.data(), V, K, T, lse[r], coef, dz.data());
-            for (int64_t v = 0; v < V; ++v)
-                for (int64_t j = 0; j < d; ++j) dhr[j] += dz[v] * W[v * d + j];
+            add_dh_row(dz.data(), W, V, d, dhr);
         }
     });
 }
@@ -252,6 +259,76 @@ void fklo_dW_rows(const double* h, const double* W, const int32_t* idx, const do
                     if (idx[i * K + k] == v) s += p[k];
                 const double c = grad_loss * T / static_cast<double>(nv) * (std::exp(z / T - lse[i]) - s);
                 for (int64_t j = 0; j < d; ++j) o[j] += c * h[i * d + j];
+            }
+        }
+    });
+}
+
+// KL + hard-label cross-entropy ("Distillyatsiya i szhatie modeley", ml-book.com,
+// section "Kak eto rabotaet: myagkie metki i temperatura": the student's loss mixes
+// the KL between the softened distributions with the ordinary cross-entropy on the
+// true labels; read as the convex mix):
+//   loss = alpha T^2 mean KL_i + (1 - alpha) mean CE_i,  CE_i = lse1_i - z_{i,label_i},
+//   lse1 the logsumexp of z at temperature 1, means over the valid rows.
+void fklo_forward_mix(const double* h, const double* W, const int32_t* idx, const double* t, const uint8_t* mask,
+                      const int32_t* label, int64_t N, int64_t d, int64_t V, int64_t K, double T, double alpha,
+                      int threads, double* lse, double* lse1, double* kl, double* ce, uint8_t* valid, double* loss,
+                      int64_t* n_valid) {
+    parallel_for(N, threads, [&](int64_t b, int64_t e) {
+        std::vector<double> z(static_cast<size_t>(V)), p(static_cast<size_t>(K));
+        for (int64_t i = b; i < e; ++i) {
+            const bool has = teacher_row(t + i * K, K, T, p.data());
+            valid[i] = row_valid(mask, i, has) ? 1 : 0;
+            forward_row(h + i * d, W, idx + i * K, p.data(), d, V, K, T, z.data(), lse + i, kl + i);
+            lse1[i] = lse_row(z.data(), V, 1.0);
+            ce[i] = lse1[i] - z[label[i]];
+        }
+    });
+    int64_t nv = 0;
+    double skl = 0.0, sce = 0.0;
+    for (int64_t i = 0; i < N; ++i) {
+        if (valid[i]) {
+            ++nv;
+            skl += kl[i];
+            sce += ce[i];
+        }
+    }
+    *n_valid = nv;
+    *loss = nv > 0 ? alpha * T * T * skl / static_cast<double>(nv) + (1.0 - alpha) * sce / static_cast<double>(nv)
+                   : 0.0;
+}
+
+// dh [N][d], dW [V][d] of the mixture times grad_loss:
+//   dz_iv = g valid_i [alpha T (q_iv - s_iv) + (1 - alpha)(q1_iv - [v = label_i])] / N_valid.
+void fklo_backward_mix(const double* h, const double* W, const int32_t* idx, const double* t, const uint8_t* mask,
+                       const int32_t* label, int64_t N, int64_t d, int64_t V, int64_t K, double T, double alpha,
+                       double grad_loss, int threads, double* dh, double* dW) {
+    std::fill(dh, dh + N * d, 0.0);
+    std::fill(dW, dW + V * d, 0.0);
+    const int64_t nv = count_valid(t, mask, N, K, T);
+    if (nv == 0) return;
+    std::vector<double> dz(static_cast<size_t>(N * V));
+    parallel_for(N, threads, [&](int64_t b, int64_t e) {
+        std::vector<double> z(static_cast<size_t>(V)), p(static_cast<size_t>(K)), q1(static_cast<size_t>(V));
+        for (int64_t i = b; i < e; ++i) {
+            const bool has = teacher_row(t + i * K, K, T, p.data());
+            const double g = row_valid(mask, i, has) ? grad_loss / static_cast<double>(nv) : 0.0;
+            double* dzr = dz.data() + i * V;
+            logit_row(h + i * d, W, d, V, z.data());
+            dz_row(z.data(), idx + i * K, p.data(), V, K, T, lse_row(z.data(), V, T), g * alpha * T, dzr);
+            const double l1 = lse_row(z.data(), V, 1.0);
+            for (int64_t v = 0; v < V; ++v) q1[v] = std::exp(z[v] - l1);
+            q1[label[i]] -= 1.0;
+            for (int64_t v = 0; v < V; ++v) dzr[v] += g * (1.0 - alpha) * q1[v];
+            add_dh_row(dzr, W, V, d, dh + i * d);
+        }
+    });
+    parallel_for(V, threads, [&](int64_t b, int64_t e) {
+        for (int64_t v = b; v < e; ++v) {
+            double* dwv = dW + v * d;
+            for (int64_t i = 0; i < N; ++i) {
+                const double c = dz[i * V + v];
+                for (int64_t j = 0; j < d; ++j) dwv[j] += c * h[i * d + j];
             }
         }
     });

@@ -95,17 +95,19 @@ CPP_MUTATIONS = {
     "teacher_ignores_T": ("bool teacher_row(const double* t, int64_t K, double T, double* p) {",
                           "bool teacher_row(const double* t, int64_t K, double T_, double* p) {\n"
                           "    const double T = 1.0;\n    (void)T_;"),
-    "student_normaliser_truncated": ("lse[i] = lse_row(z.data(), V, T);\n            kl[i]",
-                                     "lse[i] = lse_row(z.data(), K, T);\n            kl[i]"),
+    "student_normaliser_truncated": ("*lse = lse_row(z, V, T);", "*lse = lse_row(z, K, T);"),
     "gradient_sign": ("dz[v] *= coef;", "dz[v] *= -coef;"),
     "gradient_drops_teacher": ("for (int64_t k = 0; k < K; ++k) dz[idx[k]] -= p[k];", ""),
     "index_off_by_one": ("const double logq = z[idx[k]] / T - lse;",
                          "const double logq = z[idx[k] == 0 ? 1 : idx[k] - 1] / T - lse;"),
     "mean_over_all_rows": ("T * T * sum / static_cast<double>(nv)", "T * T * sum / static_cast<double>(N)"),
     "reverse_kl": ("kl += p[k] * (std::log(p[k]) - logq);", "kl += std::exp(logq) * (logq - std::log(p[k]));"),
-    "dW_rows_permuted": ("double* dwv = dW + v * d;", "double* dwv = dW + (V - 1 - v) * d;"),
+    "dW_rows_permuted": ("double* dwv = dW + v * d;\n                for (int64_t i = r0; i < r1; ++i) {",
+                         "double* dwv = dW + (V - 1 - v) * d;\n                for (int64_t i = r0; i < r1; ++i) {"),
     "lse_missing_max_shift": ("return m + std::log(s);", "return std::log(s);"),
     "dh_wrong_weight_row": ("dhi[j] += dzr[v] * W[v * d + j];", "dhi[j] += dzr[v] * W[((v + 1) % V) * d + j];"),
+    "mixture_ce_without_lse": ("ce[i] = lse1[i] - z[label[i]];", "ce[i] = -z[label[i]];"),
+    "mixture_grad_label_sign": ("q1[label[i]] -= 1.0;", "q1[label[i]] += 1.0;"),
     "topk_ascending": ("return z[a] > z[c] || (z[a] == z[c] && a < c);",
                        "return z[a] < z[c] || (z[a] == z[c] && a < c);"),
     "topk_ties_to_larger_id": ("return z[a] > z[c] || (z[a] == z[c] && a < c);",
