@@ -174,6 +174,7 @@ EDGE = [
     (260, 96, 3000, 256, 1.0, "uniform", 128),
     (300, 128, 2000, 20, 0.05, "uniform", 128),
     (300, 128, 2000, 20, 20.0, "half-student", 0),
+    (300, 4096, 1500, 16, 1.0, "uniform", 256),  # a wide hidden size: 8 wide dh / dW column tiles
 ]
 
 
