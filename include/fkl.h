@@ -195,6 +195,12 @@ size_t fkl_topk_workspace_size(int64_t N, int d, int64_t V, int K, int chunk);
 fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int64_t V, int K, int chunk,
                             int32_t* idx, float* logit, void* ws, size_t ws_bytes, void* stream);
 
+/* dh [N][d] (bf16) *= g and dW [V][d] (fp32) *= g, g = *grad (one fp32 on the
+ * device): the chain rule for gradients that fkl_forward_backward formed during
+ * the forward with grad_loss = 1, once the upstream gradient is known (autograd's
+ * backward).  g = 1 leaves both unchanged bit for bit. */
+fkl_status fkl_scale_grads(void* dh, float* dW, int64_t N, int d, int64_t V, const float* grad, void* stream);
+
 /* Synchronises `stream` and returns the device status word of `ws` (FKL_OK if
  * no device-side error was recorded since the last call that used `ws`). */
 fkl_status fkl_get_status(const void* ws, void* stream);

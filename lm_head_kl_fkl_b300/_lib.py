@@ -42,6 +42,7 @@ SIGNATURES = {
     "fkl_topk_workspace_size": (c_size, [c_i64, c_int, c_i64, c_int, c_int]),
     "fkl_teacher_topk": (c_int, [c_void_p, c_void_p, c_i64, c_int, c_i64, c_int, c_int, c_void_p, c_void_p,
                                  c_void_p, c_size, c_void_p]),
+    "fkl_scale_grads": (c_int, [c_void_p, c_void_p, c_i64, c_int, c_i64, c_void_p, c_void_p]),
     "fkl_get_status": (c_int, [c_void_p, c_void_p]),
     "fkl_status_string": (c_char_p, [c_int]),
     "fkl_last_error": (c_char_p, []),

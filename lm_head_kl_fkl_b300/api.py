@@ -235,8 +235,38 @@ class FKLLoss(torch.autograd.Function):
         return dh, dW.to(W.dtype), None, None, None, None, None
 
 
-def fkl_loss(h, W, idx, tlogit, mask=None, T: float = 1.0, chunk: int = 0) -> torch.Tensor:
-    """Autograd-aware fused loss (scalar)."""
+class FKLLossKeepLogits(torch.autograd.Function):
+    """The same loss with its gradients formed during the forward (fkl_forward_backward:
+    each chunk's logits kept instead of recomputed, 6 N d V tensor FLOP instead of 8);
+    the backward only scales them by the upstream gradient (fkl_scale_grads).  dh and
+    dW are allocated in the forward and held until the backward."""
+
+    @staticmethod
+    def forward(ctx, h, W, idx, tlogit, mask, T, chunk):
+        loss, _, dh, dW = forward_backward(h, W, idx, tlogit, mask, T, chunk=chunk)
+        ctx.save_for_backward(dh, dW)
+        ctx.w_dtype = W.dtype
+        return loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, g):
+        dh, dW = ctx.saved_tensors
+        g = g.reshape(1).to(torch.float32).contiguous()
+        N, d = dh.shape
+        st = _lib.lib().fkl_scale_grads(_ptr(dh), _ptr(dW), N, d, dW.shape[0], _ptr(g), _stream(dh.device))
+        _check(st, "fkl_scale_grads")
+        return dh, dW.to(ctx.w_dtype), None, None, None, None, None
+
+
+def fkl_loss(h, W, idx, tlogit, mask=None, T: float = 1.0, chunk: int = 0,
+             keep_logits: bool = False) -> torch.Tensor:
+    """Autograd-aware fused loss (scalar).
+
+    keep_logits=False: fkl_forward now, fkl_backward (logits recomputed) in autograd's
+    backward.  keep_logits=True: loss and gradients together in the forward, without
+    the recompute; faster, with dh and dW held from the forward to the backward."""
+    if keep_logits:
+        return FKLLossKeepLogits.apply(h, W, idx, tlogit, mask, T, chunk)
     return FKLLoss.apply(h, W, idx, tlogit, mask, T, chunk)
 
 

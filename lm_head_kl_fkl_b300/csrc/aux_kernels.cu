@@ -490,6 +490,32 @@ void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const i
                                             logit_out);
 }
 
+// dh *= g (bf16, rounded once more to nearest even) and dW *= g (fp32), with the
+// upstream gradient g read from the device: the chain rule of a loss whose
+// gradients were formed during the forward.
+__global__ void scale_grads_kernel(__nv_bfloat162* __restrict__ dh, size_t n_dh2, float4* __restrict__ dW,
+                                   size_t n_dw4, const float* __restrict__ g) {
+    const float s = *g;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_dw4; i += stride) {
+        float4 v = dW[i];
+        v.x *= s;
+        v.y *= s;
+        v.z *= s;
+        v.w *= s;
+        dW[i] = v;
+    }
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_dh2; i += stride) {
+        const float2 v = __bfloat1622float2(dh[i]);
+        dh[i] = __floats2bfloat162_rn(v.x * s, v.y * s);
+    }
+}
+
+void launch_scale_grads(void* dh, size_t n_dh, float* dW, size_t n_dw, const float* g, int grid, cudaStream_t s) {
+    scale_grads_kernel<<<grid, 256, 0, s>>>(static_cast<__nv_bfloat162*>(dh), n_dh / 2,
+                                            reinterpret_cast<float4*>(dW), n_dw / 4, g);
+}
+
 void launch_count_valid(const float* tlogit, const uint8_t* mask, int64_t N, int K, int* n_valid,
                         int grid, cudaStream_t s) {
     count_valid_kernel<<<grid, 256, 0, s>>>(tlogit, mask, N, K, n_valid);

@@ -88,7 +88,7 @@ const char* const kKindNames[KK_NUM] = {
     "count_valid", "teacher_prep", "fwd_gemm_lse", "fwd_finalize", "loss_reduce",
     "bwd_gemm_dz", "bwd_gemm_dh", "dh_reduce", "bwd_gemm_dw", "selftest_gemm",
     "fb_gemm_lse_keep", "fb_dz_from_logits",
-    "tk_gemm_tile_max", "tk_threshold", "tk_gemm_candidates", "tk_select", "selftest_wait",
+    "tk_gemm_tile_max", "tk_threshold", "tk_gemm_candidates", "tk_select", "selftest_wait", "scale_grads",
 };
 
 // ---------------------------------------------------------------- device facts
@@ -888,6 +888,18 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
         FKL_SMALL(KK_TK_SELECT, launch_topk_select(cand_v, cand_i, P.cap, cnt_gt, cnt_eq, tie_i, theta, rows, K,
                                                    idx + size_t(row0) * K, logit + size_t(row0) * K, s));
     }
+    return FKL_OK;
+}
+
+fkl_status fkl_scale_grads(void* dh, float* dW, int64_t N, int d, int64_t V, const float* grad, void* stream) {
+    g_err[0] = 0;
+    if (!dh || !dW || !grad) return fail(FKL_ERR_INVALID_ARG, "null dh, dW or grad pointer");
+    if (N < 1 || V < 1 || d < 8 || d % 8 != 0) return fail(FKL_ERR_INVALID_ARG, "N, V >= 1 and d a multiple of 8");
+    if (!aligned16(dh) || !aligned16(dW)) return fail(FKL_ERR_INVALID_ARG, "dh and dW must be 16-byte aligned");
+    if (fkl_status st = device_ready()) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FKL_SMALL(KK_SCALE_GRADS, launch_scale_grads(dh, size_t(N) * d, dW, size_t(V) * d, grad,
+                                                 device_info().sms * 8, s));
     return FKL_OK;
 }
 

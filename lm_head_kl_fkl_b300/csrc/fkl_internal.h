@@ -37,6 +37,7 @@ enum KernelKind {
     KK_TK_GEMM_CAND,   // teacher top-K: tcgen05 GEMM again, logits >= threshold appended per row
     KK_TK_SELECT,      // teacher top-K: per-row selection and sort of the candidates
     KK_SELFTEST_WAIT,  // bounded-wait self-test
+    KK_SCALE_GRADS,    // dh, dW times an upstream gradient
     KK_NUM
 };
 
@@ -126,6 +127,7 @@ void launch_topk_threshold(const float* part_m, int part_stride, int ntiles, int
 void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const int* cnt_gt, const int* cnt_eq,
                         const int* tie_i, const float* theta, int rows, int K, int32_t* idx_out, float* logit_out,
                         cudaStream_t s);
+void launch_scale_grads(void* dh, size_t n_dh, float* dW, size_t n_dw, const float* g, int grid, cudaStream_t s);
 void launch_dz_from_logits(void* yz, int64_t Vs, int64_t V, const float* part_m, int part_stride,
                            const float* lse, const uint8_t* valid, const int* n_valid, const float* grad,
                            float T, const int* sidx, const float* sp, int K, int rows, cudaStream_t s);

@@ -99,3 +99,37 @@ def test_full_size_bench_workload():
     dW_ref = oracle.dW_rows(synth.bf16_bits_to_f64(x["h"]), Wf, x["idx"], x["t"], x["mask"], x["T"], g["lse"], vr)
     dW_gpu = dW[torch.from_numpy(vr).to(dW.device)].cpu().numpy().astype(np.float64)
     assert rel_l2(dW_gpu, dW_ref) <= TOL_GRAD_REL_L2
+
+
+def test_autograd_keep_logits_matches_oracle_and_recompute():
+    x = synth.make_inputs(256, 128, 1024, 16, 2.0, 0.05, "uniform", seed=85)
+    xd = to_device(x)
+    grads = {}
+    for keep in (False, True):
+        h = xd["h"].clone().requires_grad_(True)
+        W = xd["W"].clone().requires_grad_(True)
+        loss = api.fkl_loss(h, W, xd["idx"], xd["t"], xd["mask"], 2.0, keep_logits=keep)
+        (3.0 * loss).backward()
+        grads[keep] = (loss.item(), h.grad.double().cpu().numpy(), W.grad.double().cpu().numpy())
+    hh, WW = oracle_inputs(x)
+    ref = oracle.forward(hh, WW, x["idx"], x["t"], x["mask"], 2.0)
+    g = oracle.backward(hh, WW, x["idx"], x["t"], x["mask"], 2.0, grad_loss=3.0)
+    loss, dh, dW = grads[True]
+    assert abs(loss - ref["loss"]) <= TOL_LOSS_REL * abs(ref["loss"])
+    assert rel_l2(dh, g["dh"]) <= TOL_GRAD_REL_L2 and rel_l2(dW, g["dW"]) <= TOL_GRAD_REL_L2
+    assert rel_l2(dh, grads[False][1]) <= 5e-3 and rel_l2(dW, grads[False][2]) <= 5e-3
+
+
+def test_scale_grads_by_one_is_exact():
+    x = synth.make_inputs(200, 64, 700, 8, 1.0, 0.05, "uniform", seed=86)
+    xd = to_device(x)
+    _, _, dh, dW = api.forward_backward(xd["h"], xd["W"], xd["idx"], xd["t"], xd["mask"], 1.0)
+    a, b = dh.clone(), dW.clone()
+    import ctypes
+    from lm_head_kl_fkl_b300 import _lib
+    one = torch.ones(1, dtype=torch.float32, device=dh.device)
+    st = _lib.lib().fkl_scale_grads(ctypes.c_void_p(dh.data_ptr()), ctypes.c_void_p(dW.data_ptr()), 200, 64, 700,
+                                    ctypes.c_void_p(one.data_ptr()),
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert st == 0 and torch.equal(a, dh) and torch.equal(b, dW)
