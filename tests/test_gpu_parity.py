@@ -183,3 +183,31 @@ def test_edge_sizes(shape):
     N, d, V, K, T, index, chunk = shape
     x = synth.make_inputs(N, d, V, K, T, 0.05, index, seed=9200 + N + V)
     _check(x, run_fused(to_device(x), chunk=chunk))
+
+
+def test_dW_rows_sum_to_zero():
+    """sum_v dz_iv = T (sum_v q_iv - sum_k p_ik) / N_valid = 0 for every row, so the rows of
+    dW sum to the zero vector -- up to the bf16 rounding of dz."""
+    x = synth.make_inputs(700, 96, 3000, 24, 1.5, 0.05, "zipf1.1", seed=9400)
+    out = run_fused(to_device(x), chunk=256)
+    col = out["dW"].sum(axis=0)
+    scale = np.abs(out["dW"]).sum(axis=0)
+    assert np.all(np.abs(col) <= 2e-3 * scale), float((np.abs(col) / scale).max())
+
+
+def test_uniform_student_closed_form():
+    """W = 0: every logit is 0, so lse = log V / T * T = log V and KL_i = log V - H(p_i)."""
+    x = synth.make_inputs(300, 64, 5000, 16, 2.0, 0.05, "uniform", seed=9401)
+    x["W"] = np.zeros_like(x["W"])
+    out = run_fused(to_device(x))
+    assert np.abs(out["lse"] - np.log(5000.0)).max() <= 1e-5
+    p = scipy_softmax(x["t"].astype(np.float64) / 2.0)
+    H = -(p * np.log(p)).sum(axis=1)
+    keep = x["mask"] != 0
+    ref = 4.0 * (np.log(5000.0) - H[keep]).mean()
+    assert abs(out["loss"] - ref) <= 1e-4 * abs(ref)
+
+
+def scipy_softmax(a):
+    import scipy.special
+    return scipy.special.softmax(a, axis=1)
