@@ -490,7 +490,7 @@ def run_fused(args):
     # ---- the memory-stress workload (N = 131072): peak device memory of the same call pair
     mem = None
     ws_gb = ws.numel() / 1e9
-    if not args.no_memory_stress and args.config == 3 and args.shape is None:
+    if not args.no_memory_stress and args.config == 3 and args.shape is None and world == 1:
         del h, W, idx, t, mask, ws, loss, lse, dh, dW
         if not args.no_e2e:
             del h_in, idx_in, t_in, m_in
