@@ -102,7 +102,6 @@ struct GemmParams {
 cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& tmA,
                         const CUtensorMap& tmB, const CUtensorMap& tmOut, const GemmParams& p,
                         int max_pairs, cudaStream_t stream);
-size_t gemm_smem_bytes(int bn, int b_mn, int epi);
 cudaError_t launch_wait_timeout(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 // Small kernels implemented in aux_kernels.cu.

@@ -15,9 +15,11 @@
 // 32 KB of B per 64-deep k-block for twice the MMA work of a 256-wide tile: 25 %
 // less L2->SMEM traffic per FLOP.  The 512-column accumulator fills TMEM, so it
 // is single-buffered (the epilogue does not overlap the next tile's MMAs); this
-// pays where the k-loop is long against the epilogue (dh, dW).  On the last,
-// ragged column tile the second sub-tile's N shrinks to the valid columns
-// (rounded up to 64), and both CTAs load their halves of that narrower B.
+// pays where the k-loop is long against the epilogue (dh).
+//
+// On the last, ragged column tile (of either kind) the MMA's N shrinks to the
+// valid columns rounded up to 64, and both CTAs load their halves of that
+// narrower B, so no tensor work goes to padding.
 //
 // Roles, in each CTA of the pair (192 threads, one CTA per SM):
 //   warp 0      one lane issues the CTA's TMA loads of A and B k-blocks into a
@@ -58,6 +60,7 @@
 #include <climits>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -142,12 +145,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Width of sub-tile j of column tile n: BN, except the second sub-tile of a
-// ragged last wide tile, which covers the valid columns rounded up to 64 (0 if
-// none are left).
+// Width of sub-tile j of column tile n: BN, except on the ragged last column
+// tile, where the MMA's N shrinks to the valid columns rounded up to 64 (0 if none
+// are left), so that no MMA work goes to padding (d = 2880 on 256-wide tiles would
+// otherwise waste 6.7 %).  Accumulator columns beyond the width keep stale values;
+// every epilogue reads only columns below Ncols, which the width covers.
 template <int BN, int NSUB>
 __device__ __forceinline__ int sub_width(const GemmParams& p, int n, int j) {
-    if (NSUB == 1 || j == 0) return BN;
     const int rest = p.Ncols - n * BN * NSUB - j * BN;
     if (rest >= BN) return BN;
     return rest <= 0 ? 0 : (rest + 63) & ~63;
@@ -225,8 +229,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int arow = m * 2 * kBM + static_cast<int>(rank) * kBM;
                 int bcol[NSUB];  // first B column of this CTA's half of each sub-tile
 #pragma unroll
-                for (int j = 0; j < NSUB; ++j)
-                    bcol[j] = n * TW + j * BN + static_cast<int>(rank) * (sub_width<BN, NSUB>(p, n, j) / 2);
+                for (int j = 0; j < NSUB; ++j) {
+                    const int w = sub_width<BN, NSUB>(p, n, j);
+                    bcol[j] = n * TW + j * BN + static_cast<int>(rank) * (w == BN ? BN / 2 : w / 2);
+                }
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, s_abort, p.status)) {
                         ok = false;
@@ -278,12 +284,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int kb0 = kb_begin(p, s), kb1 = kb_begin(p, s + 1);
                 const int acc = tc % NBUF;
                 const uint32_t aph = (tc / NBUF) & 1;
-                uint32_t idesc[NSUB];
                 int width[NSUB];
+                bool full = true;
 #pragma unroll
                 for (int j = 0; j < NSUB; ++j) {
                     width[j] = sub_width<BN, NSUB>(p, n, j);
-                    idesc[j] = umma_idesc_bf16(2 * kBM, width[j] > 0 ? width[j] : BN, A_MN, B_MN);
+                    full = full && width[j] == BN;
                 }
                 if (!mbar_wait(tempty0 + 8u * acc, aph ^ 1u, s_abort, p.status)) {
                     ok = false;
@@ -291,33 +297,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * 256);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(full0 + 8u * stage, phase, s_abort, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = base + stage * C::STAGE_BYTES, sb = sa + C::A_BYTES;
+                // Full tiles (all but the ragged last column tile) issue with the
+                // compile-time instruction descriptor and no width tests.
+                auto kloop = [&](auto full_tag) {
+                    constexpr bool FULL = decltype(full_tag)::value;
+                    uint32_t idesc[NSUB];
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * kk, 8192u, 1024u)
-                                                 : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
+                    for (int j = 0; j < NSUB; ++j)
+                        idesc[j] = FULL ? umma_idesc_bf16(2 * kBM, BN, A_MN, B_MN)
+                                        : umma_idesc_bf16(2 * kBM, width[j] > 0 ? width[j] : BN, A_MN, B_MN);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(full0 + 8u * stage, phase, s_abort, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = base + stage * C::STAGE_BYTES, sb = sa + C::A_BYTES;
 #pragma unroll
-                        for (int j = 0; j < NSUB; ++j) {
-                            if (width[j] == 0) continue;
-                            const uint32_t sbj = sb + j * C::B_SUB_BYTES;
-                            const uint64_t bd = B_MN ? smem_desc_sw128(sbj + 2048u * kk, 8192u, 1024u)
-                                                     : smem_desc_sw128(sbj + 32u * kk, 16u, 1024u);
-                            umma_bf16_pair(dt + static_cast<uint32_t>(j * BN), ad, bd, idesc[j],
-                                           (kb > kb0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * kk, 8192u, 1024u)
+                                                     : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
+#pragma unroll
+                            for (int j = 0; j < NSUB; ++j) {
+                                if (!FULL && width[j] == 0) continue;
+                                const uint32_t sbj = sb + j * C::B_SUB_BYTES;
+                                const uint64_t bd = B_MN ? smem_desc_sw128(sbj + 2048u * kk, 8192u, 1024u)
+                                                         : smem_desc_sw128(sbj + 32u * kk, 16u, 1024u);
+                                umma_bf16_pair(dt + static_cast<uint32_t>(j * BN), ad, bd, idesc[j],
+                                               (kb > kb0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        umma_commit_pair(empty0 + 8u * stage);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
                         }
                     }
-                    umma_commit_pair(empty0 + 8u * stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
+                };
+                if (full) kloop(std::true_type{});
+                else kloop(std::false_type{});
                 if (!ok) break;
                 umma_commit_pair(tfull0 + 8u * acc);
             }
@@ -743,20 +761,6 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, co
     const int pairs = static_cast<int>(units < resident ? units : resident);
     gemm_kernel<BN, NSUB, A_MN, B_MN, EPI><<<2 * pairs, kThreads, smem, stream>>>(tmA, tmB, tmOut, p);
     return cudaGetLastError();
-}
-
-size_t gemm_smem_bytes(int bn, int b_mn, int epi) {
-#define FKL_SMEM_CASE(BN_, NS_, B_, E_) \
-    if (bn == BN_ * NS_ && b_mn == B_ && epi == E_) return PairCfg<BN_, NS_, B_, E_>::SMEM;
-    FKL_SMEM_CASE(256, 1, 0, EPI_LSE) FKL_SMEM_CASE(256, 1, 0, EPI_DZ) FKL_SMEM_CASE(256, 1, 0, EPI_LSE_Y)
-    FKL_SMEM_CASE(256, 1, 0, EPI_TMAX) FKL_SMEM_CASE(256, 1, 0, EPI_CAND)
-    FKL_SMEM_CASE(256, 1, 0, EPI_LSE_MIX) FKL_SMEM_CASE(256, 1, 0, EPI_DZ_MIX)
-    FKL_SMEM_CASE(256, 2, 0, EPI_F32) FKL_SMEM_CASE(256, 2, 1, EPI_F32)
-    FKL_SMEM_CASE(256, 1, 0, EPI_F32) FKL_SMEM_CASE(256, 1, 1, EPI_F32)
-    FKL_SMEM_CASE(192, 1, 0, EPI_F32) FKL_SMEM_CASE(192, 1, 1, EPI_F32)
-    FKL_SMEM_CASE(128, 1, 0, EPI_F32) FKL_SMEM_CASE(128, 1, 1, EPI_F32)
-#undef FKL_SMEM_CASE
-    return 0;
 }
 
 cudaError_t launch_gemm(int bn, int a_mn, int b_mn, int epi, const CUtensorMap& tmA,
