@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # gpt-oss-20b-like workload, from an ncu capture of a smaller case scaled by the
 # units processed, keyed by the kernel source digest they were taken on (see
 # profiles/dw_gemm_traffic.md); a stale digest gives null.
-TRAFFIC = {("bwd_gemm_dw", "f43bd0d29f20"): 6.01e9}
+TRAFFIC = {("bwd_gemm_dw", "7f4ddaf280f6"): 6.01e9}
 
 
 def load_peaks():
@@ -51,10 +51,17 @@ def load_peaks():
 
 
 def kernel_digest():
+    """Hash of the GEMM kernels' code (gemm_tc.cu, ptx.cuh, fkl_internal.h) with
+    comments and blank lines removed, so that only a change of code retires
+    counters taken on an earlier build."""
+    import re
     m = hashlib.sha256()
     for f in ("gemm_tc.cu", "ptx.cuh", "fkl_internal.h"):
-        with open(os.path.join(ROOT, "lm_head_kl_fkl_b300", "csrc", f), "rb") as fh:
-            m.update(fh.read())
+        with open(os.path.join(ROOT, "lm_head_kl_fkl_b300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        m.update("\n".join(l.strip() for l in src.splitlines() if l.strip()).encode())
     return m.hexdigest()[:12]
 
 

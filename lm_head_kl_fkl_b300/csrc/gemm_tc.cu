@@ -1,4 +1,7 @@
-// Persistent 2-SM tcgen05 GEMM for sm_103a with three epilogues.
+// Persistent 2-SM tcgen05 GEMM for sm_103a and the epilogues of every
+// tensor-core pass of the library (loss forward, dz, fp32 tiles for dh and dW,
+// the kept-logits forward, the KL + CE mixture, the teacher top-K passes), plus a
+// one-thread kernel that exercises the bounded pipeline wait.
 //
 //   C[m, n] = sum_k A(m, k) B(n, k)      bf16 operands, fp32 accumulator in TMEM
 //
