@@ -23,6 +23,7 @@
 #include <vector>
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "fkl_internal.h"
 
@@ -41,6 +42,20 @@ fkl_status fail(fkl_status st, const char* fmt, ...) {
 }
 
 std::atomic<int64_t> g_launches{0};
+
+// NVTX range for profilers (a no-op unless a tool is attached): one per entry
+// point call and one per chunk.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    NvtxRange(const char* what, long long chunk) {
+        char buf[64];
+        snprintf(buf, sizeof(buf), "%s chunk %lld", what, chunk);
+        nvtxRangePushA(buf);
+    }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ---------------------------------------------------------------- profiling hooks
 struct ProfRec {
@@ -463,6 +478,7 @@ fkl_status forward_enqueue(const Plan& P, const void* h, const void* W, const in
     CUtensorMap tmW;  // B of the logit GEMM: each CTA of a pair loads 128 of the tile's 256 vocab rows
     FKL_TMAP(tmW, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, kVocabTile / 2);
     for (int64_t c = 0; c < P.n_chunks; ++c) {
+        NvtxRange nvtx_chunk("forward", static_cast<long long>(c));
         const int64_t row0 = c * P.Cc;
         const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
         FKL_SMALL(KK_TEACHER_PREP,
@@ -534,6 +550,7 @@ fkl_status backward_enqueue(const Plan& P, const void* h, const void* W, const i
     FKL_TMAP(tmW_mn, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 64);
     FKL_TMAP(tmDW, F32, dW, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32);
     for (int64_t c = 0; c < P.n_chunks; ++c) {
+        NvtxRange nvtx_chunk("backward", static_cast<long long>(c));
         const int64_t row0 = c * P.Cc;
         const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
         const double flop = 2.0 * rows * double(d) * double(V);
@@ -614,6 +631,7 @@ fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const f
                        const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T, int chunk,
                        float* loss, float* lse, void* ws, size_t ws_bytes, void* stream) {
     g_err[0] = 0;
+    NvtxRange nvtx_call("fkl_forward");
     if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
         return fail(FKL_ERR_INVALID_ARG, "%s", e);
     if (!loss || !lse) return fail(FKL_ERR_INVALID_ARG, "null loss or lse pointer");
@@ -660,6 +678,7 @@ fkl_status fkl_forward_noalloc(const void* h, const void* W, const int32_t* idx,
                                const uint8_t* mask, int64_t N, int d, int64_t V, int K, float T, int chunk,
                                float* loss, float* lse, int* status, void* stream) {
     g_err[0] = 0;
+    NvtxRange nvtx_call("fkl_forward_noalloc");
     const char* e = check_sizes(N, d, V, K, chunk);
     if (!e && (!h || !W || !idx || !tlogit)) e = "null input pointer";
     if (!e && (!(T > 0.f) || !std::isfinite(T))) e = "T must be positive and finite";
@@ -688,6 +707,7 @@ fkl_status fkl_backward(const void* h, const void* W, const int32_t* idx, const 
                         const float* lse, const float* grad_loss, void* dh, float* dW, void* ws,
                         size_t ws_bytes, void* stream) {
     g_err[0] = 0;
+    NvtxRange nvtx_call("fkl_backward");
     if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
         return fail(FKL_ERR_INVALID_ARG, "%s", e);
     if (!lse || !dh || !dW) return fail(FKL_ERR_INVALID_ARG, "null lse, dh or dW pointer");
@@ -706,6 +726,7 @@ fkl_status fkl_mix_forward(const void* h, const void* W, const int32_t* idx, con
                            float alpha, int chunk, float* loss, float* lse, float* lse1, void* ws, size_t ws_bytes,
                            void* stream) {
     g_err[0] = 0;
+    NvtxRange nvtx_call("fkl_mix_forward");
     if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
         return fail(FKL_ERR_INVALID_ARG, "%s", e);
     if (!loss || !lse || !lse1 || !label) return fail(FKL_ERR_INVALID_ARG, "null loss, lse, lse1 or label pointer");
@@ -724,6 +745,7 @@ fkl_status fkl_mix_backward(const void* h, const void* W, const int32_t* idx, co
                             float alpha, int chunk, const float* lse, const float* lse1, const float* grad_loss,
                             void* dh, float* dW, void* ws, size_t ws_bytes, void* stream) {
     g_err[0] = 0;
+    NvtxRange nvtx_call("fkl_mix_backward");
     if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
         return fail(FKL_ERR_INVALID_ARG, "%s", e);
     if (!lse || !lse1 || !label || !dh || !dW) return fail(FKL_ERR_INVALID_ARG, "null lse, lse1, label, dh or dW");
@@ -744,6 +766,7 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
                                 const float* grad_loss, float* loss, float* lse, void* dh, float* dW, void* ws,
                                 size_t ws_bytes, void* stream) {
     g_err[0] = 0;
+    NvtxRange nvtx_call("fkl_forward_backward");
     if (const char* e = check_common(h, W, idx, tlogit, N, d, V, K, T, chunk, ws))
         return fail(FKL_ERR_INVALID_ARG, "%s", e);
     if (!loss || !lse || !dh || !dW) return fail(FKL_ERR_INVALID_ARG, "null loss, lse, dh or dW pointer");
@@ -778,6 +801,7 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
     FKL_TMAP(tmW_mn, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, 64);
     FKL_TMAP(tmDW, F32, dW, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32);
     for (int64_t c = 0; c < P.n_chunks; ++c) {
+        NvtxRange nvtx_chunk("forward_backward", static_cast<long long>(c));
         const int64_t row0 = c * P.Cc;
         const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
         FKL_SMALL(KK_TEACHER_PREP,
@@ -833,6 +857,7 @@ size_t fkl_topk_workspace_size(int64_t N, int d, int64_t V, int K, int chunk) {
 fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int64_t V, int K, int chunk,
                             int32_t* idx, float* logit, void* ws, size_t ws_bytes, void* stream) {
     g_err[0] = 0;
+    NvtxRange nvtx_call("fkl_teacher_topk");
     if (!h || !W || !idx || !logit || !ws) return fail(FKL_ERR_INVALID_ARG, "null pointer");
     if (const char* e = check_sizes(N, d, V, K, chunk)) return fail(FKL_ERR_INVALID_ARG, "%s", e);
     if (!aligned16(h) || !aligned16(W) || !aligned16(ws))
@@ -857,6 +882,7 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
     CUtensorMap tmW;
     FKL_TMAP(tmW, BF16, W, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, kVocabTile / 2);
     for (int64_t c = 0; c < P.n_chunks; ++c) {
+        NvtxRange nvtx_chunk("teacher_topk", static_cast<long long>(c));
         const int64_t row0 = c * P.Cc;
         const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
         const double flop = 2.0 * rows * double(d) * double(V);
