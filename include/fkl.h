@@ -28,7 +28,8 @@
  *
  * Conventions shared by every entry point:
  *  - All array pointers are DEVICE pointers owned by the caller; the library
- *    allocates no device memory and keeps no state between calls.
+ *    allocates no device memory and keeps no state between calls (the one
+ *    exception, fkl_forward_noalloc, brings fixed scratch of its own).
  *  - Layouts are dense row-major: h [N][d] bf16, W [V][d] bf16, idx [N][K]
  *    int32, tlogit [N][K] fp32, mask [N] uint8 (NULL = every row valid),
  *    lse [N] fp32, dh [N][d] bf16, dW [V][d] fp32.
@@ -67,11 +68,12 @@ typedef enum {
     FKL_ERR_TIMEOUT = 6       /* a bounded pipeline wait gave up on the device */
 } fkl_status;
 
-/* Bytes of device workspace needed by fkl_forward and fkl_backward for these
- * sizes (chunk as passed to them).  Pure host arithmetic; 0 if the sizes are
- * invalid.  It is O(chunk * V + N): one bf16 dz chunk buffer, split-K partials
- * of dh for one chunk, the sorted teacher cache of one chunk and 4 bytes per
- * token. */
+/* Bytes of device workspace needed by fkl_forward, fkl_backward,
+ * fkl_forward_backward, fkl_mix_forward and fkl_mix_backward for these sizes
+ * (chunk as passed to them).  Pure host arithmetic; 0 if the sizes are invalid.
+ * It is O(chunk * V + N): one bf16 dz chunk buffer, split-K partials of dh for
+ * one chunk, the sorted teacher cache of one chunk and 4 bytes per token
+ * (1.79 GB at N = 131072, d = 2880, V = 201088, K = 100, default chunk). */
 size_t fkl_workspace_size(int64_t N, int d, int64_t V, int K, int chunk);
 
 /* Forward: writes loss (one fp32, device) and lse[N] (fp32, natural-log
