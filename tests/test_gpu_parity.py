@@ -175,6 +175,7 @@ EDGE = [
     (300, 128, 2000, 20, 0.05, "uniform", 128),
     (300, 128, 2000, 20, 20.0, "half-student", 0),
     (300, 4096, 1500, 16, 1.0, "uniform", 256),  # a wide hidden size: 8 wide dh / dW column tiles
+    (256, 65536, 512, 8, 1.0, "uniform", 0),     # the largest hidden size the library takes
 ]
 
 
