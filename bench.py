@@ -448,10 +448,11 @@ def run_fused(args):
         tk_kernels = per_kernel(api.profile_read(), args.steps)
         kstep = k0.elapsed_time(k1) / args.steps
         topk = {"value": N / (kstep / 1e3), "unit": "tokens/s", "ms_per_step": kstep,
-                "tflops_4NdV": 4.0 * N * d * V / (kstep / 1e3) / 1e12, "K": K,
+                "tflops_2NdV": 2.0 * N * d * V / (kstep / 1e3) / 1e12, "K": K,
                 "workspace_gb": tk_ws.numel() / 1e9, "kernels": tk_kernels,
-                "what": "fkl_teacher_topk: two tensor-core passes over z = h W^T (per-tile max, then the "
-                        "logits above the K-th largest tile max), top-K selection per row",
+                "what": "fkl_teacher_topk: one tensor-core pass over z = h W^T keeping each row's top eight "
+                        "per vocabulary tile, candidates >= the K-th largest tile max gathered from them (a second "
+                        "pass only for rows with eight or more in one tile), top-K selection per row",
                 "device_status": api.get_status(tk_ws)}
         del tk_ws
 

@@ -184,15 +184,18 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
  * paragraph 2) and "Wissensdestillation mit deutlich weniger GPU-Speicher"
  * (dailytechsnack.ch, section "Teacher-Ausgaben einmalig zwischenspeichern"),
  * in the layout fkl_forward reads (its `idx` and `tlogit`).
- * Two tensor-core passes per chunk of rows: the first keeps each row's max per
- * 256-column vocabulary tile; theta = the K-th largest of those maxima is a lower
- * bound of the row's K-th largest logit, and the logits above it lie in fewer
- * than K tiles; the second pass recomputes the logits and keeps those >= theta;
- * a last kernel selects and sorts the K largest.  Where more than K logits tie
- * at theta itself, which of them are kept is unspecified.  The full N x V
- * logits are never stored.  Conventions as above (device pointers, caller-owned,
+ * One tensor-core pass per chunk of rows keeps each row's eight largest logits
+ * per 256-column vocabulary tile.  theta = the K-th largest of the tile maxima
+ * is a lower bound of the row's K-th largest logit, and every logit >= theta
+ * lies in a tile whose max reaches it, so the candidates are gathered from the
+ * per-tile lists -- completely, unless some such tile holds eight or more logits
+ * >= theta; those rows (rare: eight of the row's top logits in one tile) get a
+ * second tensor-core pass that keeps all their logits >= theta.  A last kernel selects and sorts the K largest.  Where more than K
+ * logits tie at theta itself, which of them are kept is unspecified.  The full
+ * N x V logits are never stored.  Conventions as above (device pointers, caller-owned,
  * stream-ordered, status word at the start of ws); chunk = 0 means 1024 rows.
- * The workspace is O(chunk * min(V, 256 K)) bytes: 208 MB at V = 201088, K = 100. */
+ * The workspace is O(chunk * (min(V, 256 K) + V / 4)) bytes: 263 MB at
+ * V = 201088, K = 100. */
 size_t fkl_topk_workspace_size(int64_t N, int d, int64_t V, int K, int chunk);
 fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int64_t V, int K, int chunk,
                             int32_t* idx, float* logit, void* ws, size_t ws_bytes, void* stream);

@@ -368,6 +368,64 @@ __global__ void topk_threshold_kernel(const float* __restrict__ part_m, int stri
     }
 }
 
+// Per row (one warp): the candidates from each tile's kTopPerTile largest logits.
+// Every logit above theta lies in a tile whose max reaches theta; when such a
+// tile's last kept logit is still >= theta, the tile may hold more candidates than
+// were kept, and the row is flagged (and its lists emptied) for the second
+// tensor-core pass instead.  Unflagged rows end with every logit >= theta listed
+// (those equal to theta in the tie list, at most K of them).
+__global__ void topk_gather_kernel(const float* __restrict__ part_m, const float* __restrict__ top_v,
+                                   const int* __restrict__ top_i, int stride, int ntiles, int rows, int K,
+                                   const float* __restrict__ theta, int* __restrict__ cnt_gt,
+                                   int* __restrict__ cnt_eq, float* __restrict__ cand_v, int* __restrict__ cand_i,
+                                   int cap, int* __restrict__ tie_i, uint8_t* __restrict__ row_flag,
+                                   int* __restrict__ any_flag) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const float th = theta[r];
+    bool flag = false;
+    for (int n = lane; n < ntiles; n += 32) {
+        const size_t o = static_cast<size_t>(n) * stride + r;
+        if (!(part_m[o] >= th)) continue;
+        float v[kTopPerTile];
+        int id[kTopPerTile];
+#pragma unroll
+        for (int q4 = 0; q4 < kTopPerTile / 4; ++q4) {
+            const float4 a = reinterpret_cast<const float4*>(top_v)[o * (kTopPerTile / 4) + q4];
+            const int4 b = reinterpret_cast<const int4*>(top_i)[o * (kTopPerTile / 4) + q4];
+            v[4 * q4] = a.x, v[4 * q4 + 1] = a.y, v[4 * q4 + 2] = a.z, v[4 * q4 + 3] = a.w;
+            id[4 * q4] = b.x, id[4 * q4 + 1] = b.y, id[4 * q4 + 2] = b.z, id[4 * q4 + 3] = b.w;
+        }
+        if (v[kTopPerTile - 1] >= th) {
+            flag = true;
+            continue;
+        }
+#pragma unroll
+        for (int e = 0; e < kTopPerTile - 1; ++e) {
+            if (v[e] > th) {
+                const int slot = atomicAdd(cnt_gt + r, 1);
+                if (slot < cap) {
+                    cand_v[static_cast<size_t>(r) * cap + slot] = v[e];
+                    cand_i[static_cast<size_t>(r) * cap + slot] = id[e];
+                }
+            } else if (v[e] == th) {
+                const int slot = atomicAdd(cnt_eq + r, 1);
+                if (slot < K) tie_i[static_cast<size_t>(r) * K + slot] = id[e];
+            }
+        }
+    }
+    flag = __any_sync(0xffffffffu, flag);
+    if (lane == 0) {
+        row_flag[r] = flag ? 1 : 0;
+        if (flag) {
+            atomicExch(cnt_gt + r, 0);
+            atomicExch(cnt_eq + r, 0);
+            atomicExch(any_flag, 1);
+        }
+    }
+}
+
 // Per row (one block of 256): the K largest logits among the candidates, sorted by
 // value (descending), equal values by id (ascending).  If at least K candidates
 // are above theta, the K-th largest value is found by a bitwise search over the
@@ -481,6 +539,13 @@ __global__ void topk_select_kernel(const float* __restrict__ cand_v, const int* 
 void launch_topk_threshold(const float* part_m, int part_stride, int ntiles, int rows, int K, float* theta,
                            int* cnt_gt, int* cnt_eq, cudaStream_t s) {
     topk_threshold_kernel<<<(rows + 7) / 8, 256, 0, s>>>(part_m, part_stride, ntiles, rows, K, theta, cnt_gt, cnt_eq);
+}
+
+void launch_topk_gather(const float* part_m, const float* top_v, const int* top_i, int part_stride, int ntiles,
+                        int rows, int K, const float* theta, int* cnt_gt, int* cnt_eq, float* cand_v, int* cand_i,
+                        int cap, int* tie_i, uint8_t* row_flag, int* any_flag, cudaStream_t s) {
+    topk_gather_kernel<<<(rows + 7) / 8, 256, 0, s>>>(part_m, top_v, top_i, part_stride, ntiles, rows, K, theta,
+                                                      cnt_gt, cnt_eq, cand_v, cand_i, cap, tie_i, row_flag, any_flag);
 }
 
 void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const int* cnt_gt, const int* cnt_eq,

@@ -103,7 +103,8 @@ const char* const kKindNames[KK_NUM] = {
     "count_valid", "teacher_prep", "fwd_gemm_lse", "fwd_finalize", "loss_reduce",
     "bwd_gemm_dz", "bwd_gemm_dh", "dh_reduce", "bwd_gemm_dw", "selftest_gemm",
     "fb_gemm_lse_keep", "fb_dz_from_logits",
-    "tk_gemm_tile_max", "tk_threshold", "tk_gemm_candidates", "tk_select", "selftest_wait", "scale_grads",
+    "tk_gemm_tile_top8", "tk_threshold", "tk_gemm_candidates", "tk_select", "selftest_wait", "scale_grads",
+    "tk_gather",
 };
 
 // ---------------------------------------------------------------- device facts
@@ -310,7 +311,7 @@ constexpr int kDefaultTopkChunk = 1024;
 struct TopkPlan {
     int64_t N, V, n_chunks;
     int d, K, Cc, nt_v, cap;
-    size_t o_part, o_theta, o_gt, o_eq, o_cv, o_ci, o_tie, total;
+    size_t o_part, o_topv, o_topi, o_theta, o_gt, o_eq, o_flag, o_cv, o_ci, o_tie, total;
 };
 
 bool make_topk_plan(int64_t N, int d, int64_t V, int K, int chunk, TopkPlan& P) {
@@ -329,6 +330,12 @@ bool make_topk_plan(int64_t N, int d, int64_t V, int K, int chunk, TopkPlan& P) 
     size_t off = 256;
     P.o_part = off;
     off += align256(size_t(P.nt_v) * P.Cc * 4);
+    P.o_topv = off;
+    off += align256(size_t(P.nt_v) * P.Cc * kTopPerTile * 4);
+    P.o_topi = off;
+    off += align256(size_t(P.nt_v) * P.Cc * kTopPerTile * 4);
+    P.o_flag = off;
+    off += align256(size_t(P.Cc));
     P.o_theta = off;
     off += align256(size_t(P.Cc) * 4);
     P.o_gt = off;
@@ -870,7 +877,11 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* w = static_cast<char*>(ws);
     int* status = reinterpret_cast<int*>(w);
+    int* any_flag = status + 1;
     float* part = reinterpret_cast<float*>(w + P.o_part);
+    float* top_v = reinterpret_cast<float*>(w + P.o_topv);
+    int* top_i = reinterpret_cast<int*>(w + P.o_topi);
+    uint8_t* row_flag = reinterpret_cast<uint8_t*>(w + P.o_flag);
     float* theta = reinterpret_cast<float*>(w + P.o_theta);
     int* cnt_gt = reinterpret_cast<int*>(w + P.o_gt);
     int* cnt_eq = reinterpret_cast<int*>(w + P.o_eq);
@@ -899,10 +910,18 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
         p.Ncols = static_cast<int>(V);
         p.status = status;
         p.part_m = part;
+        p.top_v = top_v;
+        p.top_i = top_i;
         p.part_stride = P.Cc;
         p.K = K;
+        FKL_CUDA_TRY(cudaMemsetAsync(any_flag, 0, sizeof(int), s));
         if (fkl_status st = run_gemm(KK_TK_GEMM_TMAX, 256, 0, 0, EPI_TMAX, tmH, tmW, tmW, p, flop, s)) return st;
         FKL_SMALL(KK_TK_THRESHOLD, launch_topk_threshold(part, P.Cc, P.nt_v, rows, K, theta, cnt_gt, cnt_eq, s));
+        FKL_SMALL(KK_TK_GATHER, launch_topk_gather(part, top_v, top_i, P.Cc, P.nt_v, rows, K, theta, cnt_gt, cnt_eq,
+                                                   cand_v, cand_i, P.cap, tie_i, row_flag, any_flag, s));
+        // the second tensor-core pass, for the rows the gather flagged; it returns at once if none is
+        p.any_flag = any_flag;
+        p.row_flag = row_flag;
         p.theta = theta;
         p.cnt_gt = cnt_gt;
         p.cnt_eq = cnt_eq;
@@ -910,7 +929,8 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
         p.cand_i = cand_i;
         p.cand_cap = P.cap;
         p.tie_i = tie_i;
-        if (fkl_status st = run_gemm(KK_TK_GEMM_CAND, 256, 0, 0, EPI_CAND, tmH, tmW, tmW, p, flop, s)) return st;
+        // (its FLOP are not counted: the launch usually returns at once)
+        if (fkl_status st = run_gemm(KK_TK_GEMM_CAND, 256, 0, 0, EPI_CAND, tmH, tmW, tmW, p, 0.0, s)) return st;
         FKL_SMALL(KK_TK_SELECT, launch_topk_select(cand_v, cand_i, P.cap, cnt_gt, cnt_eq, tie_i, theta, rows, K,
                                                    idx + size_t(row0) * K, logit + size_t(row0) * K, s));
     }

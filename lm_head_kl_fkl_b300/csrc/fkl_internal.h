@@ -17,6 +17,7 @@ constexpr int kVocabTile = 256;   // vocabulary columns per tile in the logit GE
 constexpr int kThreads = 192;     // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr int kPlanSMs = 148;     // SM count the workspace plan is sized for (B300)
 constexpr int kMaxK = 256;        // teacher entries per token
+constexpr int kTopPerTile = 8;    // teacher top-K: largest logits kept per row and vocabulary tile
 
 // Kernel kinds, for the launch counter and the profiling hooks.
 enum KernelKind {
@@ -34,10 +35,11 @@ enum KernelKind {
     KK_FB_DZ,          // dz from the kept logits (elementwise)
     KK_TK_GEMM_TMAX,   // teacher top-K: tcgen05 GEMM, per-row max of each vocabulary tile
     KK_TK_THRESHOLD,   // teacher top-K: per-row K-th largest tile max
-    KK_TK_GEMM_CAND,   // teacher top-K: tcgen05 GEMM again, logits >= threshold appended per row
+    KK_TK_GEMM_CAND,   // teacher top-K: tcgen05 GEMM again for flagged rows (returns at once if none)
     KK_TK_SELECT,      // teacher top-K: per-row selection and sort of the candidates
     KK_SELFTEST_WAIT,  // bounded-wait self-test
     KK_SCALE_GRADS,    // dh, dW times an upstream gradient
+    KK_TK_GATHER,      // teacher top-K: candidates from the per-tile top four
     KK_NUM
 };
 
@@ -79,7 +81,13 @@ struct GemmParams {
     // EPI_F32
     int split_row_stride;  // output row offset per split (dh partials), 0 otherwise
     int reduce;            // 1: TMA reduce-add into the output, 0: TMA store
-    // EPI_TMAX writes part_m ([n_tiles][part_stride], raw logits).  EPI_CAND:
+    // EPI_TMAX writes part_m ([n_tiles][part_stride], tile max of the raw logits)
+    // and the tile's four largest logits and ids:
+    float* top_v;          // [n_tiles][part_stride][kTopPerTile]
+    int* top_i;            // [n_tiles][part_stride][kTopPerTile]
+    // EPI_CAND:
+    const int* any_flag;   // device word: non-zero if some row is flagged
+    const uint8_t* row_flag;  // [M] rows whose candidates the gather could not complete
     const float* theta;    // [M] per-row threshold
     int* cnt_gt;           // [M] logits > theta seen so far
     int* cnt_eq;           // [M] logits == theta seen so far
@@ -123,6 +131,9 @@ void launch_dh_reduce(const float* part, int splits, size_t split_elems, int row
                       cudaStream_t s);
 void launch_topk_threshold(const float* part_m, int part_stride, int ntiles, int rows, int K, float* theta,
                            int* cnt_gt, int* cnt_eq, cudaStream_t s);
+void launch_topk_gather(const float* part_m, const float* top_v, const int* top_i, int part_stride, int ntiles,
+                        int rows, int K, const float* theta, int* cnt_gt, int* cnt_eq, float* cand_v, int* cand_i,
+                        int cap, int* tie_i, uint8_t* row_flag, int* any_flag, cudaStream_t s);
 void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const int* cnt_gt, const int* cnt_eq,
                         const int* tie_i, const float* theta, int rows, int K, int32_t* idx_out, float* logit_out,
                         cudaStream_t s);

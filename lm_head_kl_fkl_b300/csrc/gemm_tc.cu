@@ -47,10 +47,13 @@
 //   EPI_LSE_MIX / EPI_DZ_MIX  the same for the KL + hard-label cross-entropy
 //            mixture: also a temperature-1 running max / sum and the logit at the
 //            row's label; dz gains (1 - alpha)/T (q_1 - onehot(label)) per row.
-//   EPI_TMAX each row's largest logit over the tile (teacher top-K, first pass).
-//   EPI_CAND every logit >= the row's threshold, appended to the row's candidate
-//            list with an atomic counter (teacher top-K, second pass); logits
-//            equal to the threshold go to a separate list of at most K ids.
+//   EPI_TMAX each row's kTopPerTile largest logits over the tile, with their
+//            ids (teacher top-K; the first of them is the tile max).
+//   EPI_CAND for the rows flagged by the top-K gather (a tile with kTopPerTile or
+//            more logits >= the row's threshold), every logit >= the threshold,
+//            appended to the row's candidate list with an atomic counter; logits
+//            equal to the threshold go to a separate list of at most K ids.  The
+//            whole launch returns at once when no row is flagged.
 //   EPI_LSE_Y  EPI_LSE for a forward whose backward follows at once: a first
 //            pass over the tile finds each row's tile max (and gathers the
 //            teacher logits), a second sums 2^(y) and keeps y = z log2e / T - max
@@ -186,6 +189,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(gbar + 16 * STAGES + 40);
     volatile int* s_abort = reinterpret_cast<volatile int*>(gbar + 16 * STAGES + 44);
 
+    if constexpr (EPI == EPI_CAND) {
+        if (*p.any_flag == 0) return;  // every CTA reads the same word: all leave, nothing was set up
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
@@ -519,7 +525,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
                 tc_fence_after();
                 const int v0 = n * BN;
-                float mt = -INFINITY;
+                // the row's kTopPerTile largest logits over the tile, descending; equal
+                // ones keep the smaller id (columns arrive in increasing order)
+                float tv[kTopPerTile];
+                int ti[kTopPerTile];
+#pragma unroll
+                for (int e = 0; e < kTopPerTile; ++e) {
+                    tv[e] = -INFINITY;
+                    ti[e] = INT_MAX;
+                }
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     const int col0 = v0 + c * 32;
@@ -528,20 +542,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     tmem_ld32(tt + c * 32, z);
                     const int nv = p.Ncols - col0;
-                    float cm0 = -INFINITY, cm1 = -INFINITY;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        cm0 = fmaxf(cm0, (j < nv) ? z[j] : -INFINITY);
-                        cm1 = fmaxf(cm1, (j + 1 < nv) ? z[j + 1] : -INFINITY);
+                    for (int j = 0; j < 32; ++j) {
+                        const float x = (j < nv) ? z[j] : -INFINITY;
+                        const int xi = col0 + j;
+                        bool gt[kTopPerTile];
+#pragma unroll
+                        for (int e = 0; e < kTopPerTile; ++e) gt[e] = x > tv[e];
+#pragma unroll
+                        for (int e = kTopPerTile - 1; e > 0; --e) {  // shift down below x's place
+                            tv[e] = gt[e - 1] ? tv[e - 1] : (gt[e] ? x : tv[e]);
+                            ti[e] = gt[e - 1] ? ti[e - 1] : (gt[e] ? xi : ti[e]);
+                        }
+                        tv[0] = gt[0] ? x : tv[0];
+                        ti[0] = gt[0] ? xi : ti[0];
                     }
-                    mt = fmaxf(mt, fmaxf(cm0, cm1));
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
-                if (row_ok) p.part_m[static_cast<size_t>(n) * p.part_stride + row] = mt;
+                if (row_ok) {
+                    const size_t o = static_cast<size_t>(n) * p.part_stride + row;
+                    p.part_m[o] = tv[0];
+                    float4* vo = reinterpret_cast<float4*>(p.top_v) + o * (kTopPerTile / 4);
+                    int4* io = reinterpret_cast<int4*>(p.top_i) + o * (kTopPerTile / 4);
+#pragma unroll
+                    for (int q4 = 0; q4 < kTopPerTile / 4; ++q4) {
+                        vo[q4] = make_float4(tv[4 * q4], tv[4 * q4 + 1], tv[4 * q4 + 2], tv[4 * q4 + 3]);
+                        io[q4] = make_int4(ti[4 * q4], ti[4 * q4 + 1], ti[4 * q4 + 2], ti[4 * q4 + 3]);
+                    }
+                }
             } else if constexpr (EPI == EPI_CAND) {
-                const float th = row_ok ? p.theta[row] : INFINITY;
+                const float th = (row_ok && p.row_flag[row]) ? p.theta[row] : INFINITY;
                 if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
                 tc_fence_after();
                 const int v0 = n * BN;

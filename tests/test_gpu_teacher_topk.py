@@ -119,3 +119,41 @@ def test_full_size_teacher_cache_rows():
     idx, val = _run(x["h"][:N], x["W"], 100)
     rows = np.sort(np.random.default_rng(7400).choice(N, 64, replace=False))
     _check(x["h"][:N], x["W"], 100, idx, val, rows=rows)
+
+
+def _run_ws(h_bits, W_bits, K):
+    """Like _run, and also the workspace's second word: non-zero if some row needed the
+    second tensor-core pass."""
+    h = torch.from_numpy(h_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    W = torch.from_numpy(W_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    ws = torch.zeros(api.topk_workspace_size(h.shape[0], h.shape[1], W.shape[0], K), dtype=torch.uint8,
+                     device="cuda")
+    idx, logit = api.teacher_topk(h, W, K, ws=ws)
+    torch.cuda.synchronize()
+    second = int(ws[4:8].view(torch.int32).item())
+    return idx.cpu().numpy().astype(np.int64), logit.cpu().numpy().astype(np.float64), second
+
+
+def test_clustered_top_logits_take_the_second_pass():
+    """Twelve ids of one vocabulary tile carry every row's largest logits, so that tile
+    holds more candidates than the eight kept per tile: the rows go through the second
+    tensor-core pass, and the result is still the exact top-K."""
+    rng = np.random.default_rng(7500)
+    N, d, V, K = 300, 64, 6000, 32
+    hf = rng.standard_normal((N, d))
+    hf[:, 0] = 4.0
+    Wf = rng.standard_normal((V, d)) / np.sqrt(d)
+    Wf[10:22, 0] = 2.5 + 0.05 * np.arange(12)
+    h, W = _bf16(hf), _bf16(Wf)
+    idx, val, second = _run_ws(h, W, K)
+    assert second == 1
+    _check(h, W, K, idx, val)
+
+
+def test_spread_top_logits_need_one_pass():
+    """Distinct logits of the gpt-oss-like head: no tile holds eight of a row's top 100,
+    the candidates come from the first pass alone."""
+    x = synth.config_inputs(3)
+    idx, val, second = _run_ws(x["h"][:1024], x["W"], 100)
+    assert second == 0
+    _check(x["h"][:1024], x["W"], 100, idx, val, rows=np.arange(0, 1024, 64))
