@@ -294,7 +294,8 @@ def run_fused(args):
 
     rank, local_rank, world = dist_env()
     if world > 1:
-        dist.init_process_group("nccl")
+        torch.cuda.set_device(local_rank)  # bind the rank's GPU before NCCL comes up
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     x, c = workload(args.config, args.shape)
