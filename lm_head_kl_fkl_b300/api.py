@@ -1,4 +1,6 @@
-"""Torch-facing API over libfkl.so: forward, backward and an autograd loss.
+"""Torch-facing API over libfkl.so: the loss's forward and backward, both in one
+call, the KL + cross-entropy mixture, the teacher top-K cache producer and the
+autograd loss.
 
 Every step of the loss runs in the library's CUDA kernels; this module only
 checks tensor properties, allocates outputs and the workspace with torch, and
