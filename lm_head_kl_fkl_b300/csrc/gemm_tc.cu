@@ -315,31 +315,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < NSUB; ++j)
                         idesc[j] = FULL ? umma_idesc_bf16(2 * kBM, BN, A_MN, B_MN)
                                         : umma_idesc_bf16(2 * kBM, width[j] > 0 ? width[j] : BN, A_MN, B_MN);
-                    for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!mbar_wait(full0 + 8u * stage, phase, s_abort, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t sa = base + stage * C::STAGE_BYTES, sb = sa + C::A_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * kk, 8192u, 1024u)
-                                                     : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
-#pragma unroll
-                            for (int j = 0; j < NSUB; ++j) {
-                                if (!FULL && width[j] == 0) continue;
-                                const uint32_t sbj = sb + j * C::B_SUB_BYTES;
-                                const uint64_t bd = B_MN ? smem_desc_sw128(sbj + 2048u * kk, 8192u, 1024u)
-                                                         : smem_desc_sw128(sbj + 32u * kk, 16u, 1024u);
-                                umma_bf16_pair(dt + static_cast<uint32_t>(j * BN), ad, bd, idesc[j],
-                                               (kb > kb0 || kk > 0) ? 1u : 0u);
+                    if constexpr (FULL && NSUB == 1) {
+                        // One asm block per k-block (umma_kblock_pair), which also
+                        // tests whether the next stage has landed: when it has, the
+                        // next k-block starts without a barrier round trip.  The
+                        // descriptors of stage s are those of stage 0 plus
+                        // s * STAGE_BYTES / 16 (the address field is linear below
+                        // 256 KB).
+                        const uint64_t ad0 = A_MN ? smem_desc_sw128(base, 8192u, 1024u)
+                                                  : smem_desc_sw128(base, 16u, 1024u);
+                        const uint64_t bd0 = B_MN ? smem_desc_sw128(base + C::A_BYTES, 8192u, 1024u)
+                                                  : smem_desc_sw128(base + C::A_BYTES, 16u, 1024u);
+                        constexpr uint32_t KA = A_MN ? 2048u / 16u : 32u / 16u;
+                        constexpr uint32_t KB = B_MN ? 2048u / 16u : 32u / 16u;
+                        bool landed = false;
+                        for (int kb = kb0; kb < kb1; ++kb) {
+                            if (!landed && !mbar_wait(full0 + 8u * stage, phase, s_abort, p.status)) {
+                                ok = false;
+                                break;
                             }
+                            tc_fence_after();
+                            const uint64_t soff = static_cast<uint64_t>(stage) * (C::STAGE_BYTES >> 4);
+                            int nstage = stage + 1;
+                            uint32_t nphase = phase;
+                            if (nstage == STAGES) {
+                                nstage = 0;
+                                nphase ^= 1u;
+                            }
+                            landed = umma_kblock_pair<KA, KB>(dt, ad0 + soff, bd0 + soff, idesc[0],
+                                                              kb > kb0 ? 1u : 0u, empty0 + 8u * stage,
+                                                              full0 + 8u * nstage, nphase) != 0;
+                            stage = nstage;
+                            phase = nphase;
                         }
-                        umma_commit_pair(empty0 + 8u * stage);
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
+                    } else {
+                        for (int kb = kb0; kb < kb1; ++kb) {
+                            if (!mbar_wait(full0 + 8u * stage, phase, s_abort, p.status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t sa = base + stage * C::STAGE_BYTES, sb = sa + C::A_BYTES;
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk) {
+                                const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048u * kk, 8192u, 1024u)
+                                                         : smem_desc_sw128(sa + 32u * kk, 16u, 1024u);
+#pragma unroll
+                                for (int j = 0; j < NSUB; ++j) {
+                                    if (!FULL && width[j] == 0) continue;
+                                    const uint32_t sbj = sb + j * C::B_SUB_BYTES;
+                                    const uint64_t bd = B_MN ? smem_desc_sw128(sbj + 2048u * kk, 8192u, 1024u)
+                                                             : smem_desc_sw128(sbj + 32u * kk, 16u, 1024u);
+                                    umma_bf16_pair(dt + static_cast<uint32_t>(j * BN), ad, bd, idesc[j],
+                                                   (kb > kb0 || kk > 0) ? 1u : 0u);
+                                }
+                            }
+                            umma_commit_pair(empty0 + 8u * stage);
+                            if (++stage == STAGES) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
                         }
                     }
                 };

@@ -267,6 +267,40 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
         : "memory");
 }
 
+// One 64-deep k-block of a 256-column pair tile: four K = 16 MMAs whose operand
+// descriptors advance by KA / KB (the descriptor units of 16 k-elements), then the
+// commit that frees the stage in both CTAs.  Before them, a non-blocking test of
+// the next stage's `full` barrier; its result is read only after the commit, so
+// its shared-memory latency overlaps the MMA issue instead of preceding the next
+// k-block.  Returns 1 if the next stage had already landed.
+template <uint32_t KA, uint32_t KB>
+__device__ __forceinline__ uint32_t umma_kblock_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                     uint32_t idesc, uint32_t accumulate, uint32_t empty_bar,
+                                                     uint32_t next_full_bar, uint32_t next_parity) {
+    uint32_t ready;
+    const uint16_t both = 0x3;
+    asm volatile(
+        "{\n\t.reg .pred acc, one, landed;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 landed, [%7], %8;\n\t"
+        "setp.ne.b32 acc, %5, 0;\n\t"
+        "setp.ne.b32 one, %10, 0;\n\t"
+        "add.s64 a1, %2, %11;\n\tadd.s64 b1, %3, %14;\n\t"
+        "add.s64 a2, %2, %12;\n\tadd.s64 b2, %3, %15;\n\t"
+        "add.s64 a3, %2, %13;\n\tadd.s64 b3, %3, %16;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %4, acc;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a1, b1, %4, one;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a2, b2, %4, one;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a3, b3, %4, one;\n\t"
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%6], %9;\n\t"
+        "selp.u32 %0, 1, 0, landed;\n\t}"
+        : "=r"(ready)
+        : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(empty_bar),
+          "r"(next_full_bar), "r"(next_parity), "h"(both), "r"(1u), "n"(KA), "n"(2 * KA), "n"(3 * KA),
+          "n"(KB), "n"(2 * KB), "n"(3 * KB)
+        : "memory");
+    return ready;
+}
+
 // ---------------------------------------------------------------- scalar helpers
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
