@@ -222,7 +222,8 @@ const char* fkl_last_error(void);
  * recorded events and reports, per kernel kind k < n, the summed device time in
  * ms, the number of launches and the algorithmic FLOP those launches performed
  * (tensor-core kernels only; 0 otherwise); it returns the number of kinds.
- * fkl_profile_reset forgets the records.  Not thread-safe. */
+ * fkl_profile_reset forgets the records.  Safe to call from several host
+ * threads; a launch is timed if profiling was on when it started. */
 void fkl_profile_enable(int on);
 void fkl_profile_reset(void);
 int fkl_profile_read(double* ms, int64_t* launches, double* flop, int n);

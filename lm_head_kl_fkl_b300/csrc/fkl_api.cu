@@ -63,11 +63,13 @@ struct ProfRec {
     double flop;
     cudaEvent_t a, b;
 };
-bool g_prof_on = false;
+// Records and spare events are shared by every calling thread: g_prof_mu guards both.
+std::atomic<bool> g_prof_on{false};
+std::mutex g_prof_mu;
 std::vector<ProfRec> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
 
-cudaEvent_t pool_event() {
+cudaEvent_t pool_event() {  // caller holds g_prof_mu
     if (!g_event_pool.empty()) {
         cudaEvent_t e = g_event_pool.back();
         g_event_pool.pop_back();
@@ -84,16 +86,25 @@ struct LaunchScope {
     LaunchScope(int kind, double flop, cudaStream_t st) : s(st) {
         rec.kind = kind;
         rec.flop = flop;
-        if (g_prof_on) {
-            rec.a = pool_event();
-            rec.b = pool_event();
-            cudaEventRecord(rec.a, s);
+        if (g_prof_on.load()) {
+            {
+                std::lock_guard<std::mutex> lock(g_prof_mu);
+                rec.a = pool_event();
+                rec.b = pool_event();
+                if (!rec.a || !rec.b) {  // event creation failed: this launch goes untimed
+                    if (rec.a) g_event_pool.push_back(rec.a);
+                    if (rec.b) g_event_pool.push_back(rec.b);
+                    rec.a = rec.b = nullptr;
+                }
+            }
+            if (rec.a && rec.b) cudaEventRecord(rec.a, s);
         }
     }
     ~LaunchScope() {
         ++g_launches;
-        if (g_prof_on) {
+        if (rec.a && rec.b) {  // profiled at the start of this launch
             cudaEventRecord(rec.b, s);
+            std::lock_guard<std::mutex> lock(g_prof_mu);
             g_prof.push_back(rec);
         }
     }
@@ -959,9 +970,10 @@ fkl_status fkl_get_status(const void* ws, void* stream) {
     return static_cast<fkl_status>(st);
 }
 
-void fkl_profile_enable(int on) { g_prof_on = on != 0; }
+void fkl_profile_enable(int on) { g_prof_on.store(on != 0); }
 
 void fkl_profile_reset(void) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
     for (auto& r : g_prof) {
         g_event_pool.push_back(r.a);
         g_event_pool.push_back(r.b);
@@ -975,6 +987,7 @@ int fkl_profile_read(double* ms, int64_t* launches, double* flop, int n) {
         if (launches) launches[k] = 0;
         if (flop) flop[k] = 0;
     }
+    std::lock_guard<std::mutex> lock(g_prof_mu);
     for (auto& r : g_prof) {
         if (r.kind >= n) continue;
         float t = 0.f;
