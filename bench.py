@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # gpt-oss-20b-like workload, from an ncu capture of a smaller case scaled by the
 # units processed, keyed by the kernel source digest they were taken on (see
 # profiles/dw_gemm_traffic.md); a stale digest gives null.
-TRAFFIC = {("bwd_gemm_dw", "48fdda725e32"): 6.00e9}
+TRAFFIC = {("bwd_gemm_dw", "fb0246ca0473"): 5.99e9}
 
 
 def load_peaks():

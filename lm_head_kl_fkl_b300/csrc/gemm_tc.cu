@@ -316,37 +316,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         idesc[j] = FULL ? umma_idesc_bf16(2 * kBM, BN, A_MN, B_MN)
                                         : umma_idesc_bf16(2 * kBM, width[j] > 0 ? width[j] : BN, A_MN, B_MN);
                     if constexpr (FULL && NSUB == 1) {
-                        // One asm block per k-block (umma_kblock_pair), which also
-                        // tests whether the next stage has landed: when it has, the
-                        // next k-block starts without a barrier round trip.  The
-                        // descriptors of stage s are those of stage 0 plus
-                        // s * STAGE_BYTES / 16 (the address field is linear below
-                        // 256 KB).
+                        // k-blocks go in pairs, each pair from one asm block
+                        // (umma_2kblocks_pair; an odd last one from umma_kblock_pair)
+                        // that also tests, without blocking, whether the stages after
+                        // it have landed: when they have, the next pair starts without
+                        // a barrier round trip.  The descriptors of stage s are those
+                        // of stage 0 plus s * STAGE_BYTES / 16 (the address field is
+                        // linear below 256 KB).
+                        static_assert(STAGES >= 4, "two stages issued and two tested are distinct");
                         const uint64_t ad0 = A_MN ? smem_desc_sw128(base, 8192u, 1024u)
                                                   : smem_desc_sw128(base, 16u, 1024u);
                         const uint64_t bd0 = B_MN ? smem_desc_sw128(base + C::A_BYTES, 8192u, 1024u)
                                                   : smem_desc_sw128(base + C::A_BYTES, 16u, 1024u);
                         constexpr uint32_t KA = A_MN ? 2048u / 16u : 32u / 16u;
                         constexpr uint32_t KB = B_MN ? 2048u / 16u : 32u / 16u;
-                        bool landed = false;
-                        for (int kb = kb0; kb < kb1; ++kb) {
-                            if (!landed && !mbar_wait(full0 + 8u * stage, phase, s_abort, p.status)) {
+                        constexpr uint64_t kStageDesc = C::STAGE_BYTES >> 4;
+                        auto next = [](int st, uint32_t ph, int& nst, uint32_t& nph) {
+                            nst = st + 1 == STAGES ? 0 : st + 1;
+                            nph = st + 1 == STAGES ? ph ^ 1u : ph;
+                        };
+                        bool landed = false;  // the stages this iteration uses are known to have landed
+                        int kb = kb0;
+                        for (; kb + 1 < kb1; kb += 2) {
+                            int s1, s2, s3;
+                            uint32_t p1, p2, p3;
+                            next(stage, phase, s1, p1);
+                            next(s1, p1, s2, p2);
+                            next(s2, p2, s3, p3);
+                            if (!landed && (!mbar_wait(full0 + 8u * stage, phase, s_abort, p.status) ||
+                                            !mbar_wait(full0 + 8u * s1, p1, s_abort, p.status))) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            const uint64_t soff = static_cast<uint64_t>(stage) * (C::STAGE_BYTES >> 4);
-                            int nstage = stage + 1;
-                            uint32_t nphase = phase;
-                            if (nstage == STAGES) {
-                                nstage = 0;
-                                nphase ^= 1u;
+                            const uint64_t o0 = static_cast<uint64_t>(stage) * kStageDesc;
+                            const uint64_t o1 = static_cast<uint64_t>(s1) * kStageDesc;
+                            landed = umma_2kblocks_pair<KA, KB>(dt, ad0 + o0, bd0 + o0, ad0 + o1, bd0 + o1, idesc[0],
+                                                                kb > kb0 ? 1u : 0u, empty0 + 8u * stage,
+                                                                empty0 + 8u * s1, full0 + 8u * s2, p2,
+                                                                full0 + 8u * s3, p3) != 0;
+                            stage = s2;
+                            phase = p2;
+                        }
+                        if (ok && kb < kb1) {
+                            int s1;
+                            uint32_t p1;
+                            next(stage, phase, s1, p1);
+                            if (!landed && !mbar_wait(full0 + 8u * stage, phase, s_abort, p.status)) {
+                                ok = false;
+                                return;
                             }
-                            landed = umma_kblock_pair<KA, KB>(dt, ad0 + soff, bd0 + soff, idesc[0],
-                                                              kb > kb0 ? 1u : 0u, empty0 + 8u * stage,
-                                                              full0 + 8u * nstage, nphase) != 0;
-                            stage = nstage;
-                            phase = nphase;
+                            tc_fence_after();
+                            const uint64_t o0 = static_cast<uint64_t>(stage) * kStageDesc;
+                            umma_kblock_pair<KA, KB>(dt, ad0 + o0, bd0 + o0, idesc[0], kb > kb0 ? 1u : 0u,
+                                                     empty0 + 8u * stage, full0 + 8u * s1, p1);
+                            stage = s1;
+                            phase = p1;
                         }
                     } else {
                         for (int kb = kb0; kb < kb1; ++kb) {

@@ -301,6 +301,51 @@ __device__ __forceinline__ uint32_t umma_kblock_pair(uint32_t d_tmem, uint64_t a
     return ready;
 }
 
+// Two consecutive k-blocks (stages s0 and s1) as above: eight MMAs, one commit
+// freeing each stage, and non-blocking tests of the two stages after them.
+// Returns 1 if both of those had landed.  Halves the issuing thread's fixed cost
+// (loop, fence, barrier test) per MMA against umma_kblock_pair.
+template <uint32_t KA, uint32_t KB>
+__device__ __forceinline__ uint32_t umma_2kblocks_pair(uint32_t d_tmem, uint64_t a0_desc, uint64_t b0_desc,
+                                                       uint64_t a1_desc, uint64_t b1_desc, uint32_t idesc,
+                                                       uint32_t accumulate, uint32_t empty0_bar,
+                                                       uint32_t empty1_bar, uint32_t full2_bar,
+                                                       uint32_t parity2, uint32_t full3_bar, uint32_t parity3) {
+    uint32_t ready;
+    const uint16_t both = 0x3;
+    asm volatile(
+        "{\n\t.reg .pred acc, one, l2, l3;\n\t"
+        ".reg .b64 a01, a02, a03, b01, b02, b03, a11, a12, a13, b11, b12, b13;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 l2, [%10], %11;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 l3, [%12], %13;\n\t"
+        "setp.ne.b32 acc, %7, 0;\n\t"
+        "setp.ne.b32 one, %15, 0;\n\t"
+        "add.s64 a01, %1, %16;\n\tadd.s64 b01, %2, %19;\n\t"
+        "add.s64 a02, %1, %17;\n\tadd.s64 b02, %2, %20;\n\t"
+        "add.s64 a03, %1, %18;\n\tadd.s64 b03, %2, %21;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%5], %1, %2, %6, acc;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%5], a01, b01, %6, one;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%5], a02, b02, %6, one;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%5], a03, b03, %6, one;\n\t"
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%8], %14;\n\t"
+        "add.s64 a11, %3, %16;\n\tadd.s64 b11, %4, %19;\n\t"
+        "add.s64 a12, %3, %17;\n\tadd.s64 b12, %4, %20;\n\t"
+        "add.s64 a13, %3, %18;\n\tadd.s64 b13, %4, %21;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%5], %3, %4, %6, one;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%5], a11, b11, %6, one;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%5], a12, b12, %6, one;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%5], a13, b13, %6, one;\n\t"
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%9], %14;\n\t"
+        "and.pred l2, l2, l3;\n\t"
+        "selp.u32 %0, 1, 0, l2;\n\t}"
+        : "=r"(ready)
+        : "l"(a0_desc), "l"(b0_desc), "l"(a1_desc), "l"(b1_desc), "r"(d_tmem), "r"(idesc), "r"(accumulate),
+          "r"(empty0_bar), "r"(empty1_bar), "r"(full2_bar), "r"(parity2), "r"(full3_bar), "r"(parity3),
+          "h"(both), "r"(1u), "n"(KA), "n"(2 * KA), "n"(3 * KA), "n"(KB), "n"(2 * KB), "n"(3 * KB)
+        : "memory");
+    return ready;
+}
+
 // ---------------------------------------------------------------- scalar helpers
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
