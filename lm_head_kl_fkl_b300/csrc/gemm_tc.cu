@@ -32,7 +32,10 @@
 //   warp 1      allocates 512 TMEM columns (two 256-column accumulators, or one
 //               512-column accumulator for wide tiles) for the pair; in
 //               the even CTA one lane issues the MMAs, commits `empty` (stage
-//               reusable) and `tfull` (accumulator complete) to both CTAs;
+//               reusable) and `tfull` (accumulator complete) to both CTAs.  This
+//               one thread paces the 256-wide tiles, so their k-blocks go out in
+//               pairs, eight MMAs per asm block, with the next stages' barriers
+//               tested without blocking inside the same block;
 //   warps 2-5   the epilogue: each warp drains its 32 TMEM lanes (= 32 output
 //               rows) with tcgen05.ld and reports the buffer free on the even
 //               CTA's `tempty` barrier, so the next tile's MMAs overlap it.
