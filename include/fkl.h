@@ -34,10 +34,10 @@
  *    int32, tlogit [N][K] fp32, mask [N] uint8 (NULL = every row valid),
  *    lse [N] fp32, dh [N][d] bf16, dW [V][d] fp32.
  *  - Preconditions checked on the host (FKL_ERR_INVALID_ARG, before any launch):
- *    non-NULL required pointers; N >= 1; 8 <= d, d % 8 == 0; V >= 1, V % 8 == 0
- *    is NOT required; 1 <= K <= 256, K <= V; T > 0 and finite; chunk == 0
- *    (library default) or a positive multiple of 128; h, W, dh, dW and the
- *    workspace 16-byte aligned.  Teacher ids within a row must be distinct
+ *    non-NULL required pointers; 1 <= N <= 2^40; 8 <= d <= 65536, d % 8 == 0;
+ *    1 <= V <= 2^30 (V % 8 == 0 is NOT required); 1 <= K <= 256, K <= V; T > 0
+ *    and finite; chunk == 0 (library default) or a positive multiple of 128 up
+ *    to 2^20; h, W, dh, dW and the workspace 16-byte aligned.  Teacher ids within a row must be distinct
  *    (not checked; repeated ids are summed into s).
  *  - Calls enqueue on `stream` (a cudaStream_t; NULL = legacy default stream)
  *    and return without synchronising.  Errors found on the device (a teacher
