@@ -47,6 +47,9 @@
  *    (FKL_ERR_WORKSPACE otherwise).  The same workspace may serve the forward
  *    and the backward call; its contents between calls carry no meaning except
  *    the status word.
+ *  - Host threads: calls from several threads at once, on their own streams,
+ *    are safe as long as no workspace or output is shared between calls whose
+ *    work overlaps on the GPU (per-device set-up is done once, under a lock).
  */
 #ifndef FKL_H
 #define FKL_H
@@ -190,9 +193,10 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
  * lies in a tile whose max reaches it, so the candidates are gathered from the
  * per-tile lists -- completely, unless some such tile holds eight or more logits
  * >= theta; those rows (rare: eight of the row's top logits in one tile) get a
- * second tensor-core pass that keeps all their logits >= theta.  A last kernel selects and sorts the K largest.  Where more than K
- * logits tie at theta itself, which of them are kept is unspecified.  The full
- * N x V logits are never stored.  Conventions as above (device pointers, caller-owned,
+ * second tensor-core pass that keeps all their logits >= theta.  A last kernel
+ * selects and sorts the K largest.  Where more than K logits tie at theta
+ * itself, which of them are kept is unspecified.  The full N x V logits are
+ * never stored.  Conventions as above (device pointers, caller-owned,
  * stream-ordered, status word at the start of ws); chunk = 0 means 1024 rows.
  * The workspace is O(chunk * (min(V, 256 K) + V / 4)) bytes: 263 MB at
  * V = 201088, K = 100. */
@@ -236,8 +240,8 @@ int64_t fkl_launch_count(void);
  * pipeline the loss kernels use.  a_mn = 0: A is [M][K] row-major (K-major);
  * a_mn = 1: A is stored [K][M] (M-major).  b_mn = 0: B is [N][K]; b_mn = 1: B
  * is stored [K][N].  bn selects the N tile: 256, 192 or 128 (double-buffered
- * accumulators), or 512 (two 256-wide sub-tiles sharing A, single-buffered).  M, N, K >= 1 and
- * multiples of 8.  `ws` (>= 256 bytes, device) receives the status word.  Used
+ * accumulators), or 512 (two 256-wide sub-tiles sharing A, single-buffered).
+ * M, N, K >= 1 and multiples of 8.  `ws` (>= 256 bytes, device) receives the status word.  Used
  * to check the operand descriptors in isolation. */
 fkl_status fkl_selftest_gemm(const void* A, const void* B, float* C, int M, int N, int K,
                              int a_mn, int b_mn, int bn, void* ws, void* stream);
