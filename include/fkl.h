@@ -103,10 +103,14 @@ fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const f
  *    bytes (each term rounded up to 256) for chunk C (0 = 4096, capped at N
  *    rounded up to 128); beyond FKL_NOALLOC_SCRATCH_BYTES the call returns
  *    FKL_ERR_WORKSPACE before any launch, with the sizes in fkl_last_error.  At
- *    V = 201088, K = 100 and C = 4096 that is about 42 MB + 4*N.
+ *    V = 201088, K = 100 and C = 4096 that is about 42 MB + 4*N.  The 4*N
+ *    bytes do not depend on the chunk: from about 16 million rows on no chunk
+ *    fits, and the message names N as the limit.
  *  - Set-up: the first call on each device looks up the scratch's device
  *    address (with that device current).  Make that first call before any
- *    stream capture.
+ *    stream capture.  Later calls whose stream is not capturing look the
+ *    address up again (a cheap query), so that it stays right after the
+ *    device's context has been destroyed and rebuilt (cudaDeviceReset).
  *  - Sharing: every call on a device uses the same scratch, which keeps the
  *    previous call's contents (the call clears what must start at zero).  Calls
  *    whose work overlaps on the GPU -- on different streams, or from different

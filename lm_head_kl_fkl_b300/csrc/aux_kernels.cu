@@ -263,7 +263,7 @@ __global__ void dh_reduce_kernel(const float4* __restrict__ part, int splits, si
 // - s) in bf16, written over y in place.  One block per row: the y at the teacher
 // ids are read first, then the whole row is rewritten, then the teacher entries
 // (each run of equal ids once, its p summed) are written with s subtracted.
-__global__ void dz_from_logits_kernel(uint16_t* __restrict__ yz, int64_t Vs, int64_t V,
+__global__ void dz_from_logits_kernel(uint16_t* __restrict__ yz, int64_t pstride, int64_t V,
                                       const float* __restrict__ part_m, int stride,
                                       const float* __restrict__ lse, const uint8_t* __restrict__ valid,
                                       const int* __restrict__ n_valid, const float* __restrict__ grad, float T,
@@ -271,7 +271,9 @@ __global__ void dz_from_logits_kernel(uint16_t* __restrict__ yz, int64_t Vs, int
     __shared__ float s_y[kMaxK];
     constexpr float kLog2eF = 1.4426950408889634f;
     const int r = blockIdx.x;
-    uint16_t* row = yz + static_cast<size_t>(r) * Vs;
+    // element (r, v) of the panel layout: panel v / 64, row r, column v % 64
+    uint16_t* row = yz + static_cast<size_t>(r) * 64;
+    auto at = [&](int64_t v) -> uint16_t* { return row + (v >> 6) * pstride + (v & 63); };
     const int* ids = sidx + static_cast<size_t>(r) * K;
     const float* ps = sp + static_cast<size_t>(r) * K;
     const float lse2 = lse[r] * kLog2eF;
@@ -279,12 +281,13 @@ __global__ void dz_from_logits_kernel(uint16_t* __restrict__ yz, int64_t Vs, int
     const float coef = (valid[r] && nv > 0) ? T * (grad ? *grad : 1.f) / static_cast<float>(nv) : 0.f;
     for (int k = threadIdx.x; k < K; k += blockDim.x) {
         const int v = ids[k];
-        s_y[k] = (v < V) ? __half2float(__ushort_as_half(row[v])) + part_m[static_cast<size_t>(v >> 8) * stride + r]
+        s_y[k] = (v < V) ? __half2float(__ushort_as_half(*at(v))) + part_m[static_cast<size_t>(v >> 8) * stride + r]
                          : 0.f;
     }
     __syncthreads();
     for (int64_t v = static_cast<int64_t>(threadIdx.x) * 8; v < V; v += static_cast<int64_t>(blockDim.x) * 8) {
-        const uint4 in = *reinterpret_cast<const uint4*>(row + v);
+        uint4* p8 = reinterpret_cast<uint4*>(at(v));  // 8 columns inside one panel
+        const uint4 in = *p8;
         const float shift = part_m[static_cast<size_t>(v >> 8) * stride + r] - lse2;
         const uint32_t w[4] = {in.x, in.y, in.z, in.w};
         uint32_t o[4];
@@ -296,7 +299,7 @@ __global__ void dz_from_logits_kernel(uint16_t* __restrict__ yz, int64_t Vs, int
             const __nv_bfloat162 ab = __floats2bfloat162_rn(a, b);
             o[j] = *reinterpret_cast<const uint32_t*>(&ab);
         }
-        *reinterpret_cast<uint4*>(row + v) = make_uint4(o[0], o[1], o[2], o[3]);
+        *p8 = make_uint4(o[0], o[1], o[2], o[3]);
     }
     __syncthreads();
     for (int k = threadIdx.x; k < K; k += blockDim.x) {
@@ -305,15 +308,46 @@ __global__ void dz_from_logits_kernel(uint16_t* __restrict__ yz, int64_t Vs, int
         float s = ps[k];
         for (int j = k + 1; j < K && ids[j] == v; ++j) s += ps[j];
         const __nv_bfloat16 d = __float2bfloat16_rn(coef * (exp2f(s_y[k] - lse2) - s));
-        row[v] = __bfloat16_as_ushort(d);
+        *at(v) = __bfloat16_as_ushort(d);
     }
 }
 
-void launch_dz_from_logits(void* yz, int64_t Vs, int64_t V, const float* part_m, int part_stride,
+void launch_dz_from_logits(void* yz, int64_t pstride, int64_t V, const float* part_m, int part_stride,
                            const float* lse, const uint8_t* valid, const int* n_valid, const float* grad,
                            float T, const int* sidx, const float* sp, int K, int rows, cudaStream_t s) {
-    dz_from_logits_kernel<<<rows, 256, 0, s>>>(static_cast<uint16_t*>(yz), Vs, V, part_m, part_stride, lse, valid,
-                                               n_valid, grad, T, sidx, sp, K);
+    dz_from_logits_kernel<<<rows, 256, 0, s>>>(static_cast<uint16_t*>(yz), pstride, V, part_m, part_stride, lse,
+                                               valid, n_valid, grad, T, sidx, sp, K);
+}
+
+// ---------------------------------------------------------------- h transposed
+// hT[c][r] = h[r][c] over one chunk's rows (row stride of hT: ld elements): the
+// dW GEMM reads h as a K-major operand.  64 x 64 tiles through shared memory,
+// two columns per thread on the loads and two rows per thread on the stores.
+__global__ void transpose_h_kernel(const uint32_t* __restrict__ h, int rows, int d, uint32_t* __restrict__ hT,
+                                   int64_t ld) {
+    __shared__ uint16_t tile[64][66];
+    const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    for (int i = ty; i < 64; i += 8) {
+        const int r = r0 + i, c = c0 + 2 * tx;
+        uint32_t w = 0;
+        if (r < rows && c < d) w = h[(static_cast<size_t>(r) * d + c) >> 1];
+        tile[i][2 * tx] = static_cast<uint16_t>(w & 0xffffu);
+        tile[i][2 * tx + 1] = static_cast<uint16_t>(w >> 16);
+    }
+    __syncthreads();
+    for (int i = ty; i < 64; i += 8) {
+        const int c = c0 + i, r = r0 + 2 * tx;
+        if (c < d && r < rows)  // for an odd row count the pair's second half is a zero beyond the map
+            hT[(static_cast<size_t>(c) * ld + r) >> 1] =
+                static_cast<uint32_t>(tile[2 * tx][i]) | (static_cast<uint32_t>(tile[2 * tx + 1][i]) << 16);
+    }
+}
+
+void launch_transpose_h(const void* h, int rows, int d, void* hT, int64_t ld, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>((d + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+    transpose_h_kernel<<<grid, dim3(32, 8), 0, s>>>(static_cast<const uint32_t*>(h), rows, d,
+                                                    static_cast<uint32_t*>(hT), ld);
 }
 
 // ---------------------------------------------------------------- teacher top-K
@@ -326,103 +360,222 @@ __device__ __forceinline__ float unkey(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Per row (one warp): theta = the K-th largest of its per-tile maxima, or -inf
-// when there are fewer than K tiles.  At least K logits of the row are >= theta
-// (each of the K tiles contributes its max), and every logit > theta lies in one of
-// the < K tiles whose max exceeds theta, so at most (K - 1) * 256 logits are above
-// it.  Also clears the row's candidate counters.
-__global__ void topk_threshold_kernel(const float* __restrict__ part_m, int stride, int ntiles, int rows, int K,
-                                      float* __restrict__ theta, int* __restrict__ cnt_gt,
-                                      int* __restrict__ cnt_eq) {
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (r >= rows) return;
-    float th = -INFINITY;
-    if (ntiles >= K) {
-        // the row's tile maxima, lane-strided, in registers (up to 32 x kTh of them),
-        // the rest re-read from memory on each step of the search
-        constexpr int kTh = 32;
-        uint32_t key[kTh];
+// Sum over the warp (every lane gets the total).
+__device__ __forceinline__ int warp_sum(int c) {
 #pragma unroll
-        for (int j = 0; j < kTh; ++j) {
-            const int n = lane + 32 * j;
-            key[j] = n < ntiles ? fkey(part_m[static_cast<size_t>(n) * stride + r]) : 0u;
-        }
-        uint32_t t = 0;  // largest key with at least K tile maxima at or above it
-        for (int b = 31; b >= 0; --b) {
-            const uint32_t cand = t | (1u << b);
-            int c = 0;
-#pragma unroll
-            for (int j = 0; j < kTh; ++j) c += key[j] >= cand;
-            for (int n = lane + 32 * kTh; n < ntiles; n += 32)
-                c += fkey(part_m[static_cast<size_t>(n) * stride + r]) >= cand;
-            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-            if (c >= K) t = cand;
-        }
-        th = unkey(t);
-    }
-    if (lane == 0) {
-        theta[r] = th;
-        cnt_gt[r] = 0;
-        cnt_eq[r] = 0;
-    }
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    return c;
 }
 
-// Per row (one warp): the candidates from each tile's kTopPerTile largest logits.
-// Every logit above theta lies in a tile whose max reaches theta; when such a
-// tile's last kept logit is still >= theta, the tile may hold more candidates than
-// were kept, and the row is flagged (and its lists emptied) for the second
-// tensor-core pass instead.  Unflagged rows end with every logit >= theta listed
-// (those equal to theta in the tie list, at most K of them).
-__global__ void topk_gather_kernel(const float* __restrict__ part_m, const float* __restrict__ top_v,
-                                   const int* __restrict__ top_i, int stride, int ntiles, int rows, int K,
-                                   const float* __restrict__ theta, int* __restrict__ cnt_gt,
-                                   int* __restrict__ cnt_eq, float* __restrict__ cand_v, int* __restrict__ cand_i,
-                                   int cap, int* __restrict__ tie_i, uint8_t* __restrict__ row_flag,
-                                   int* __restrict__ any_flag) {
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (r >= rows) return;
-    const float th = theta[r];
+// theta of row r (one warp): the K-th largest of its per-tile maxima, or -inf when
+// there are fewer than K tiles.  At least K logits of the row are >= theta (each of
+// the K tiles contributes its max), and every logit > theta lies in one of the < K
+// tiles whose max exceeds theta, so at most (K - 1) * 256 logits are above it.
+__device__ __forceinline__ float row_theta(const float* __restrict__ part_m, int stride, int ntiles, int r, int K,
+                                           int lane) {
+    if (ntiles < K) return -INFINITY;
+    // the row's tile maxima, lane-strided, in registers (up to 32 x kTh of them),
+    // the rest re-read from memory on each step of the search
+    constexpr int kTh = 32;
+    uint32_t key[kTh];
+#pragma unroll
+    for (int j = 0; j < kTh; ++j) {
+        const int n = lane + 32 * j;
+        key[j] = n < ntiles ? fkey(part_m[static_cast<size_t>(n) * stride + r]) : 0u;
+    }
+    uint32_t t = 0;  // largest key with at least K tile maxima at or above it
+    for (int b = 31; b >= 0; --b) {
+        const uint32_t cand = t | (1u << b);
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < kTh; ++j) c += key[j] >= cand;
+        for (int n = lane + 32 * kTh; n < ntiles; n += 32)
+            c += fkey(part_m[static_cast<size_t>(n) * stride + r]) >= cand;
+        if (warp_sum(c) >= K) t = cand;
+    }
+    return unkey(t);
+}
+
+// Teacher top-K of one row per warp, from the first tensor-core pass's per-tile
+// top eight: theta (as above), then the candidates -- every kept logit > theta of
+// the tiles whose max reaches theta, and up to K logits == theta -- compacted into
+// shared memory, then the K largest (ties at the K-th value by the smallest ids)
+// sorted by value descending, ids ascending, and written out.  A tile whose eighth
+// kept logit is still >= theta may hold more candidates than were kept; such a row
+// (or one with more than kTopCap candidates) is flagged instead -- theta stored,
+// its counters cleared, nothing written -- for the second tensor-core pass and
+// topk_select_kernel.
+constexpr int kTopCap = 512;     // candidates > theta held in shared memory per row
+constexpr int kRowsPerBlock = 4;  // one warp per row
+
+__global__ void __launch_bounds__(32 * kRowsPerBlock)
+    topk_rows_kernel(const float* __restrict__ part_m, const float* __restrict__ top_v,
+                     const int* __restrict__ top_i, int stride, int ntiles, int rows, int K,
+                     float* __restrict__ theta, int* __restrict__ cnt_gt, int* __restrict__ cnt_eq,
+                     uint8_t* __restrict__ row_flag, int* __restrict__ any_flag, int32_t* __restrict__ idx_out,
+                     float* __restrict__ logit_out) {
+    __shared__ uint32_t s_key[kRowsPerBlock][kTopCap];
+    __shared__ int s_id[kRowsPerBlock][kTopCap];
+    __shared__ int s_tie[kRowsPerBlock][kMaxK];
+    __shared__ uint32_t s_skey[kRowsPerBlock][kMaxK];
+    __shared__ int s_sid[kRowsPerBlock][kMaxK];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int r = blockIdx.x * kRowsPerBlock + w;
+    if (r >= rows) return;  // whole warps only; no block-wide barrier follows
+    const unsigned lt = (1u << lane) - 1u;
+    const float th = row_theta(part_m, stride, ntiles, r, K, lane);
+
+    // gather: lanes take tiles in turn; ballots keep the lists in tile order
+    int n_gt = 0, n_eq = 0;
     bool flag = false;
-    for (int n = lane; n < ntiles; n += 32) {
-        const size_t o = static_cast<size_t>(n) * stride + r;
-        if (!(part_m[o] >= th)) continue;
+    const int nround = (ntiles + 31) & ~31;
+    for (int n0 = 0; n0 < nround; n0 += 32) {
+        const int n = n0 + lane;
         float v[kTopPerTile];
         int id[kTopPerTile];
+        const size_t o = static_cast<size_t>(n) * stride + r;
+        const bool hit = n < ntiles && part_m[o] >= th;
 #pragma unroll
-        for (int q4 = 0; q4 < kTopPerTile / 4; ++q4) {
-            const float4 a = reinterpret_cast<const float4*>(top_v)[o * (kTopPerTile / 4) + q4];
-            const int4 b = reinterpret_cast<const int4*>(top_i)[o * (kTopPerTile / 4) + q4];
-            v[4 * q4] = a.x, v[4 * q4 + 1] = a.y, v[4 * q4 + 2] = a.z, v[4 * q4 + 3] = a.w;
-            id[4 * q4] = b.x, id[4 * q4 + 1] = b.y, id[4 * q4 + 2] = b.z, id[4 * q4 + 3] = b.w;
+        for (int e = 0; e < kTopPerTile; ++e) {
+            v[e] = -INFINITY;
+            id[e] = INT_MAX;
         }
-        if (v[kTopPerTile - 1] >= th) {
+        if (hit) {
+#pragma unroll
+            for (int q4 = 0; q4 < kTopPerTile / 4; ++q4) {
+                const float4 a = reinterpret_cast<const float4*>(top_v)[o * (kTopPerTile / 4) + q4];
+                const int4 b = reinterpret_cast<const int4*>(top_i)[o * (kTopPerTile / 4) + q4];
+                v[4 * q4] = a.x, v[4 * q4 + 1] = a.y, v[4 * q4 + 2] = a.z, v[4 * q4 + 3] = a.w;
+                id[4 * q4] = b.x, id[4 * q4 + 1] = b.y, id[4 * q4 + 2] = b.z, id[4 * q4 + 3] = b.w;
+            }
+            flag = flag || v[kTopPerTile - 1] >= th;
+        }
+        if (__any_sync(0xffffffffu, flag)) {
             flag = true;
-            continue;
+            break;
         }
 #pragma unroll
         for (int e = 0; e < kTopPerTile - 1; ++e) {
-            if (v[e] > th) {
-                const int slot = atomicAdd(cnt_gt + r, 1);
-                if (slot < cap) {
-                    cand_v[static_cast<size_t>(r) * cap + slot] = v[e];
-                    cand_i[static_cast<size_t>(r) * cap + slot] = id[e];
+            const bool gt = hit && v[e] > th, eq = hit && v[e] == th;
+            const unsigned mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
+            if (gt) {
+                const int slot = n_gt + __popc(mg & lt);
+                if (slot < kTopCap) {
+                    s_key[w][slot] = fkey(v[e]);
+                    s_id[w][slot] = id[e];
                 }
-            } else if (v[e] == th) {
-                const int slot = atomicAdd(cnt_eq + r, 1);
-                if (slot < K) tie_i[static_cast<size_t>(r) * K + slot] = id[e];
             }
+            if (eq) {
+                const int slot = n_eq + __popc(me & lt);
+                if (slot < K) s_tie[w][slot] = id[e];
+            }
+            n_gt += __popc(mg);
+            n_eq += __popc(me);
         }
     }
-    flag = __any_sync(0xffffffffu, flag);
-    if (lane == 0) {
-        row_flag[r] = flag ? 1 : 0;
-        if (flag) {
-            atomicExch(cnt_gt + r, 0);
-            atomicExch(cnt_eq + r, 0);
+    if (flag || n_gt > kTopCap) {
+        if (lane == 0) {
+            theta[r] = th;
+            cnt_gt[r] = 0;
+            cnt_eq[r] = 0;
+            row_flag[r] = 1;
             atomicExch(any_flag, 1);
         }
+        return;
+    }
+    if (lane == 0) row_flag[r] = 0;
+    __syncwarp();
+
+    // selection into s_skey / s_sid [0, K)
+    if (n_gt >= K) {
+        uint32_t t = 0;  // key of the K-th largest candidate
+        for (int b = 31; b >= 0; --b) {
+            const uint32_t cand = t | (1u << b);
+            int c = 0;
+            for (int i = lane; i < n_gt; i += 32) c += s_key[w][i] >= cand;
+            if (warp_sum(c) >= K) t = cand;
+        }
+        int above = 0, at = 0;
+        for (int i = lane; i < n_gt; i += 32) {
+            above += s_key[w][i] > t;
+            at += s_key[w][i] == t;
+        }
+        above = warp_sum(above);
+        at = warp_sum(at);
+        const int need = K - above;  // candidates at the K-th value to keep, smallest ids first
+        uint32_t cut = 0x7fffffffu;  // keep the ties with id <= cut
+        if (at > need) {
+            cut = 0;
+            for (int b = 30; b >= 0; --b) {
+                const uint32_t c2 = cut | (1u << b);
+                int c = 0;
+                for (int i = lane; i < n_gt; i += 32)
+                    c += s_key[w][i] == t && static_cast<uint32_t>(s_id[w][i]) < c2;
+                if (warp_sum(c) < need) cut = c2;
+            }
+        }
+        int m = 0;
+        const int nr = (n_gt + 31) & ~31;
+        for (int i0 = 0; i0 < nr; i0 += 32) {
+            const int i = i0 + lane;
+            bool keep = false;
+            uint32_t kk = 0;
+            int ii = 0;
+            if (i < n_gt) {
+                kk = s_key[w][i];
+                ii = s_id[w][i];
+                keep = kk > t || (kk == t && static_cast<uint32_t>(ii) <= cut);
+            }
+            const unsigned mk = __ballot_sync(0xffffffffu, keep);
+            if (keep) {
+                const int slot = m + __popc(mk & lt);
+                s_skey[w][slot] = kk;
+                s_sid[w][slot] = ii;
+            }
+            m += __popc(mk);
+        }
+    } else {
+        const uint32_t tk = fkey(th);
+        for (int i = lane; i < n_gt; i += 32) {
+            s_skey[w][i] = s_key[w][i];
+            s_sid[w][i] = s_id[w][i];
+        }
+        for (int i = lane; i < K - n_gt; i += 32) {  // at least K - n_gt ties exist (K tiles reach theta)
+            s_skey[w][n_gt + i] = tk;
+            s_sid[w][n_gt + i] = s_tie[w][i];
+        }
+    }
+    int P = 1;
+    while (P < K) P <<= 1;
+    for (int i = K + lane; i < P; i += 32) {
+        s_skey[w][i] = 0u;  // below every real key: sorts last
+        s_sid[w][i] = INT_MAX;
+    }
+    __syncwarp();
+    // bitonic sort of the P slots: key descending, id ascending
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int str = size >> 1; str > 0; str >>= 1) {
+            for (int i = lane; i < P; i += 32) {
+                const int j = i ^ str;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;
+                    const uint32_t ki = s_skey[w][i], kj = s_skey[w][j];
+                    const int ii = s_sid[w][i], ij = s_sid[w][j];
+                    const bool i_first = ki > kj || (ki == kj && ii < ij);
+                    if (i_first != desc) {
+                        s_skey[w][i] = kj;
+                        s_skey[w][j] = ki;
+                        s_sid[w][i] = ij;
+                        s_sid[w][j] = ii;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    }
+    for (int k = lane; k < K; k += 32) {
+        idx_out[static_cast<size_t>(r) * K + k] = s_sid[w][k];
+        logit_out[static_cast<size_t>(r) * K + k] = unkey(s_skey[w][k]);
     }
 }
 
@@ -434,12 +587,14 @@ __global__ void topk_gather_kernel(const float* __restrict__ part_m, const float
 // theta from the tie list.
 __global__ void topk_select_kernel(const float* __restrict__ cand_v, const int* __restrict__ cand_i, int cap,
                                    const int* __restrict__ cnt_gt, const int* __restrict__ cnt_eq,
-                                   const int* __restrict__ tie_i, const float* __restrict__ theta, int K,
-                                   int32_t* __restrict__ idx_out, float* __restrict__ logit_out) {
+                                   const int* __restrict__ tie_i, const float* __restrict__ theta,
+                                   const uint8_t* __restrict__ row_flag, int K, int32_t* __restrict__ idx_out,
+                                   float* __restrict__ logit_out) {
     __shared__ uint32_t s_key[kMaxK];
     __shared__ int s_id[kMaxK];
     __shared__ int s_n;
     const int r = blockIdx.x;
+    if (!row_flag[r]) return;  // completed by topk_rows_kernel (uniform over the block)
     const float* v = cand_v + static_cast<size_t>(r) * cap;
     const int* id = cand_i + static_cast<size_t>(r) * cap;
     const int n = min(cnt_gt[r], cap);
@@ -536,23 +691,19 @@ __global__ void topk_select_kernel(const float* __restrict__ cand_v, const int* 
     }
 }
 
-void launch_topk_threshold(const float* part_m, int part_stride, int ntiles, int rows, int K, float* theta,
-                           int* cnt_gt, int* cnt_eq, cudaStream_t s) {
-    topk_threshold_kernel<<<(rows + 7) / 8, 256, 0, s>>>(part_m, part_stride, ntiles, rows, K, theta, cnt_gt, cnt_eq);
-}
-
-void launch_topk_gather(const float* part_m, const float* top_v, const int* top_i, int part_stride, int ntiles,
-                        int rows, int K, const float* theta, int* cnt_gt, int* cnt_eq, float* cand_v, int* cand_i,
-                        int cap, int* tie_i, uint8_t* row_flag, int* any_flag, cudaStream_t s) {
-    topk_gather_kernel<<<(rows + 7) / 8, 256, 0, s>>>(part_m, top_v, top_i, part_stride, ntiles, rows, K, theta,
-                                                      cnt_gt, cnt_eq, cand_v, cand_i, cap, tie_i, row_flag, any_flag);
-}
-
 void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const int* cnt_gt, const int* cnt_eq,
-                        const int* tie_i, const float* theta, int rows, int K, int32_t* idx_out, float* logit_out,
-                        cudaStream_t s) {
-    topk_select_kernel<<<rows, 256, 0, s>>>(cand_v, cand_i, cap, cnt_gt, cnt_eq, tie_i, theta, K, idx_out,
+                        const int* tie_i, const float* theta, const uint8_t* row_flag, int rows, int K,
+                        int32_t* idx_out, float* logit_out, cudaStream_t s) {
+    topk_select_kernel<<<rows, 256, 0, s>>>(cand_v, cand_i, cap, cnt_gt, cnt_eq, tie_i, theta, row_flag, K, idx_out,
                                             logit_out);
+}
+
+void launch_topk_rows(const float* part_m, const float* top_v, const int* top_i, int part_stride, int ntiles,
+                      int rows, int K, float* theta, int* cnt_gt, int* cnt_eq, uint8_t* row_flag, int* any_flag,
+                      int32_t* idx_out, float* logit_out, cudaStream_t s) {
+    topk_rows_kernel<<<(rows + kRowsPerBlock - 1) / kRowsPerBlock, 32 * kRowsPerBlock, 0, s>>>(
+        part_m, top_v, top_i, part_stride, ntiles, rows, K, theta, cnt_gt, cnt_eq, row_flag, any_flag, idx_out,
+        logit_out);
 }
 
 // dh *= g (bf16, rounded once more to nearest even) and dW *= g (fp32), with the

@@ -114,8 +114,8 @@ const char* const kKindNames[KK_NUM] = {
     "count_valid", "teacher_prep", "fwd_gemm_lse", "fwd_finalize", "loss_reduce",
     "bwd_gemm_dz", "bwd_gemm_dh", "dh_reduce", "bwd_gemm_dw", "selftest_gemm",
     "fb_gemm_lse_keep", "fb_dz_from_logits",
-    "tk_gemm_tile_top8", "tk_threshold", "tk_gemm_candidates", "tk_select", "selftest_wait", "scale_grads",
-    "tk_gather",
+    "tk_gemm_tile_top8", "tk_rows", "tk_gemm_candidates", "tk_select_flagged", "selftest_wait", "scale_grads",
+    "transpose_h",
 };
 
 // ---------------------------------------------------------------- device facts
@@ -198,6 +198,22 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
     return r == CUDA_SUCCESS;
 }
 
+// 3-D tiled tensor map of the dz panel buffer: {64 columns, rows, panel}, the
+// panels `panel_bytes` apart, each a [rows][64] bf16 (or fp16) array; 128-byte
+// swizzle.  Every box {64, box_rows, 1} is one contiguous run of box_rows x 128 bytes.
+bool make_panel_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t rows, uint64_t panels,
+                     uint64_t panel_bytes, uint32_t box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64, rows, panels};
+    cuuint64_t strides[2] = {128, panel_bytes};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- the plan
 constexpr int kDefaultChunk = 4096;
 constexpr int kMaxChunk = 1 << 20;
@@ -206,9 +222,9 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Plan {
-    int64_t N, V, Vs, n_chunks;
+    int64_t N, V, npan, n_chunks;  // npan: 64-column panels of the dz buffer
     int d, K, Cc, nt_v, bn_dh, nt_dh, bn_dw, nt_dw, splits;
-    size_t o_sidx, o_sp, o_H, o_valid, o_rowloss, o_big, o_part_dh, total;
+    size_t o_sidx, o_sp, o_H, o_valid, o_rowloss, o_big, o_part_dh, o_hT, total;
     size_t fwd_total;  // bytes the forward alone touches (a prefix of the workspace)
 };
 
@@ -289,7 +305,7 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
     P.nt_dh = static_cast<int>(cdiv(d, P.bn_dh));
     P.nt_dw = static_cast<int>(cdiv(d, P.bn_dw));
     P.splits = pick_splits(static_cast<int>(cdiv(P.Cc, kPairRows)), P.nt_dh, cdiv(V, kBK));
-    P.Vs = cdiv(V, 8) * 8;
+    P.npan = cdiv(V, 64);
     size_t off = 256;  // header: status word, N_valid
     P.o_sidx = off;
     off += align256(size_t(P.Cc) * K * 4);
@@ -303,13 +319,15 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
     off += align256(size_t(N) * 4);
     P.o_big = off;
     const size_t part_fwd = 3 * align256(size_t(P.nt_v) * P.Cc * 4);
-    const size_t dz = align256(size_t(P.Cc) * P.Vs * 2);
-    const size_t part_dh = size_t(P.splits) * P.Cc * d * 4;
+    const size_t dz = align256(size_t(P.Cc) * P.npan * 64 * 2);
+    const size_t part_dh = align256(size_t(P.splits) * P.Cc * d * 4);
     P.o_part_dh = P.o_big + dz;
     // fkl_forward keeps its partials at o_big; fkl_backward puts dz there and
     // the dh partials after it; fkl_forward_backward needs dz and the forward
-    // partials at once, so its partials share the dh partials' place.
-    P.total = P.o_big + dz + std::max(part_fwd, part_dh);
+    // partials at once, so its partials share the dh partials' place.  The
+    // chunk's h transposed (for the dW GEMM) comes last.
+    P.o_hT = P.o_big + dz + std::max(part_fwd, part_dh);
+    P.total = P.o_hT + align256(size_t(P.Cc) * d * 2);
     P.fwd_total = P.o_big + part_fwd;
     // the KL + cross-entropy mixture's forward keeps six partial arrays, not three
     P.total = std::max(P.total, P.o_big + 2 * part_fwd);
@@ -404,6 +422,14 @@ fkl_status run_gemm(int kind, int bn, int a_mn, int b_mn, int epi, const CUtenso
             return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for " #m);   \
     } while (0)
 
+// Panel map of the chunk's dz (or kept-logit) buffer with boxes of box_rows rows.
+#define FKL_PANEL_TMAP(m, dt, base, box_rows)                                                       \
+    do {                                                                                            \
+        if (!make_panel_tmap(&(m), dt, base, uint64_t(rows), uint64_t(P.npan), uint64_t(P.Cc) * 128, \
+                             box_rows))                                                             \
+            return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for " #m);                     \
+    } while (0)
+
 #define FKL_SMALL(kind, call)                                                                     \
     do {                                                                                          \
         {                                                                                         \
@@ -420,14 +446,16 @@ constexpr auto BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 constexpr auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 constexpr auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 
-// dh and dW of chunk c from its dz ([rows][Vs] bf16 in the workspace):
+// dh and dW of chunk c from its dz (bf16 in the workspace, 64-column panels of
+// [rows][64]) and its h transposed (hT, [d][Cc] bf16):
 //   dh partials [split][rows][d] = dz[:, split's V range] W[split's V range, :],
 //   their fixed-order sum in bf16 into dh_chunk, and
 //   dW (+)= dz^T h_chunk (TMA store for chunk 0, reduce-add after; one owner per
 //   output tile, chunks in stream order).
 fkl_status grads_from_dz(const Plan& P, int64_t c, int rows, const CUtensorMap& tmDz_k, const CUtensorMap& tmDz_mn,
-                         const CUtensorMap& tmH_mn, const CUtensorMap& tmW_mn, const CUtensorMap& tmPart,
-                         const CUtensorMap& tmDW, float* part, void* dh_chunk, int* status, cudaStream_t s) {
+                         const CUtensorMap& tmHT_k, const CUtensorMap& tmH_mn, const CUtensorMap& tmW_mn,
+                         const CUtensorMap& tmPart, const CUtensorMap& tmDW, float* part, void* dh_chunk, int* status,
+                         cudaStream_t s) {
     const int d = P.d;
     const double flop = 2.0 * rows * double(d) * double(P.V);
     GemmParams q{};
@@ -437,6 +465,7 @@ fkl_status grads_from_dz(const Plan& P, int64_t c, int rows, const CUtensorMap& 
     q.kb_total = static_cast<int>(cdiv(P.V, kBK));
     q.m_fastest = 0;  // pairs in flight cover every d tile of a few row tiles: dz is read once
     q.M = rows;
+    q.a_panel = 1;
     q.Ncols = d;
     q.status = status;
     q.split_row_stride = P.Cc;
@@ -451,10 +480,13 @@ fkl_status grads_from_dz(const Plan& P, int64_t c, int rows, const CUtensorMap& 
     r.kb_total = static_cast<int>(cdiv(rows, kBK));
     r.m_fastest = 0;
     r.M = static_cast<int>(P.V);
+    r.a_panel = 1;
     r.Ncols = d;
     r.status = status;
     r.reduce = c > 0 ? 1 : 0;
-    return run_gemm(KK_BWD_DW, P.bn_dw, 1, 1, EPI_F32, tmDz_mn, tmH_mn, tmDW, r, flop, s);
+    if (getenv("FKL_DW_B_MN"))  // experiment: h as an MN-major operand
+        return run_gemm(KK_BWD_DW, P.bn_dw, 1, 1, EPI_F32, tmDz_mn, tmH_mn, tmDW, r, flop, s);
+    return run_gemm(KK_BWD_DW, P.bn_dw, 1, 0, EPI_F32, tmDz_mn, tmHT_k, tmDW, r, flop, s);
 }
 
 // The forward's launch sequence on a workspace of at least P.fwd_total bytes
@@ -558,6 +590,7 @@ fkl_status backward_enqueue(const Plan& P, const void* h, const void* W, const i
     uint8_t* valid = reinterpret_cast<uint8_t*>(w + P.o_valid);
     void* dz = w + P.o_big;
     float* part = reinterpret_cast<float*>(w + P.o_part_dh);
+    void* hT = w + P.o_hT;
 
     FKL_CUDA_TRY(cudaMemsetAsync(w, 0, 256, s));
     const int sms = device_info().sms;
@@ -575,13 +608,17 @@ fkl_status backward_enqueue(const Plan& P, const void* h, const void* W, const i
         FKL_SMALL(KK_TEACHER_PREP,
                   launch_teacher_prep(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status, s));
         const char* hc = static_cast<const char*>(h) + size_t(row0) * d * 2;
-        CUtensorMap tmH_k, tmH_mn, tmDz_st, tmDz_k, tmDz_mn, tmPart;
+        CUtensorMap tmH_k, tmH_mn, tmHT_k, tmDz_st, tmDz_k, tmDz_mn, tmPart;
         FKL_TMAP(tmH_k, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 128);
         FKL_TMAP(tmH_mn, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 64);
-        FKL_TMAP(tmDz_st, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 32);
-        FKL_TMAP(tmDz_k, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 128);
-        FKL_TMAP(tmDz_mn, BF16, dz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 64);
+        // the dW GEMM's B operand: each CTA of a pair loads half of a (sub-)tile's columns of d
+        FKL_TMAP(tmHT_k, BF16, hT, uint64_t(rows), uint64_t(d), uint64_t(P.Cc) * 2, 64,
+                 uint32_t(std::min(P.bn_dw, 256) / 2));
+        FKL_PANEL_TMAP(tmDz_st, BF16, dz, 32);
+        FKL_PANEL_TMAP(tmDz_k, BF16, dz, 128);
+        FKL_PANEL_TMAP(tmDz_mn, BF16, dz, 64);
         FKL_TMAP(tmPart, F32, part, uint64_t(d), uint64_t(P.splits) * P.Cc, uint64_t(d) * 4, 32, 32);
+        FKL_SMALL(KK_TRANSPOSE_H, launch_transpose_h(hc, rows, d, hT, P.Cc, s));
 
         // dz = T g (q - s) / N_valid for this chunk's rows, bf16 [rows][V]
         GemmParams p{};
@@ -611,7 +648,7 @@ fkl_status backward_enqueue(const Plan& P, const void* h, const void* W, const i
                                      flop, s))
             return st;
 
-        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmH_mn, tmW_mn, tmPart, tmDW, part,
+        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmHT_k, tmH_mn, tmW_mn, tmPart, tmDW, part,
                                           static_cast<char*>(dh) + size_t(row0) * d * 2, status, s))
             return st;
     }
@@ -668,10 +705,13 @@ fkl_status fkl_forward(const void* h, const void* W, const int32_t* idx, const f
 // forward clears it itself.
 static __device__ __align__(256) unsigned char g_fwd_scratch[FKL_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_fwd_scratch on the current device, looked up once per
-// device.  In host code `g_fwd_scratch` names a host-side stand-in, never the
-// device memory, so kernels are only ever given this looked-up address.
-static fkl_status noalloc_scratch(void** out) {
+// Device address of g_fwd_scratch on the current device.  In host code
+// `g_fwd_scratch` names a host-side stand-in, never the device memory, so kernels
+// are only ever given this looked-up address.  The first call on a device looks
+// it up (and must come before any stream capture); the lookup is repeated on every
+// later call whose stream is not capturing (it is cheap), so that a context that
+// was destroyed and rebuilt (cudaDeviceReset) never leaves a stale address behind.
+static fkl_status noalloc_scratch(cudaStream_t s, void** out) {
     constexpr int kMaxDevices = 256;
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
@@ -679,14 +719,24 @@ static fkl_status noalloc_scratch(void** out) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(FKL_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return fail(FKL_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        cs = cudaStreamCaptureStatusActive;  // cannot tell: treat as capturing
+    }
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (cs == cudaStreamCaptureStatusNone) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_fwd_scratch);
         if (e != cudaSuccess || !p)
             return fail(FKL_ERR_CUDA, "cudaGetSymbolAddress of the forward scratch on device %d: %s", dev,
                         cudaGetErrorString(e));
         addr[dev] = p;
+    } else if (!addr[dev]) {
+        return fail(FKL_ERR_UNSUPPORTED,
+                    "the first fkl_forward_noalloc call on device %d came during stream capture: make one call "
+                    "outside capture first, so that the scratch's address can be looked up",
+                    dev);
     }
     *out = addr[dev];
     return FKL_OK;
@@ -705,16 +755,26 @@ fkl_status fkl_forward_noalloc(const void* h, const void* W, const int32_t* idx,
     if (!loss || !lse) return fail(FKL_ERR_INVALID_ARG, "null loss or lse pointer");
     Plan P;
     make_plan(N, d, V, K, chunk, P);
-    if (P.fwd_total > FKL_NOALLOC_SCRATCH_BYTES)
+    if (P.fwd_total > FKL_NOALLOC_SCRATCH_BYTES) {
+        Plan Pmin;  // the smallest chunk: if even that does not fit, the 4 bytes per row are the limit
+        make_plan(N, d, V, K, kBM, Pmin);
+        if (Pmin.fwd_total > FKL_NOALLOC_SCRATCH_BYTES)
+            return fail(FKL_ERR_WORKSPACE,
+                        "the forward needs %zu bytes of scratch for N=%lld, V=%lld, K=%d even at the smallest "
+                        "chunk (128), of which %lld grow with N (4 per row); the built-in scratch holds %zu: "
+                        "pass fewer rows per call, or use fkl_forward with a caller workspace",
+                        Pmin.fwd_total, static_cast<long long>(N), static_cast<long long>(V), K,
+                        static_cast<long long>(N) * 4, static_cast<size_t>(FKL_NOALLOC_SCRATCH_BYTES));
         return fail(FKL_ERR_WORKSPACE,
                     "the forward needs %zu bytes of scratch for N=%lld, V=%lld, K=%d, chunk=%d; the built-in "
                     "scratch holds %zu: pass a smaller chunk, or use fkl_forward with a caller workspace",
                     P.fwd_total, static_cast<long long>(N), static_cast<long long>(V), K, P.Cc,
                     static_cast<size_t>(FKL_NOALLOC_SCRATCH_BYTES));
+    }
     if (fkl_status st = device_ready()) return st;
-    void* scratch = nullptr;
-    if (fkl_status st = noalloc_scratch(&scratch)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* scratch = nullptr;
+    if (fkl_status st = noalloc_scratch(s, &scratch)) return st;
     if (fkl_status st = forward_enqueue(P, h, W, idx, tlogit, mask, T, loss, lse, scratch, s)) return st;
     if (status) FKL_CUDA_TRY(cudaMemcpyAsync(status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, s));
     return FKL_OK;
@@ -805,6 +865,7 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
     float* rowloss = reinterpret_cast<float*>(w + P.o_rowloss);
     void* yz = w + P.o_big;  // kept logits (fp16), then dz (bf16) in place
     float* part = reinterpret_cast<float*>(w + P.o_part_dh);
+    void* hT = w + P.o_hT;
     const size_t pstride = align256(size_t(P.nt_v) * P.Cc * 4);
     float* pm = reinterpret_cast<float*>(w + P.o_part_dh);  // forward partials share the dh partials' place
     float* pl = reinterpret_cast<float*>(w + P.o_part_dh + pstride);
@@ -825,13 +886,17 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
         FKL_SMALL(KK_TEACHER_PREP,
                   launch_teacher_prep(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status, s));
         const char* hc = static_cast<const char*>(h) + size_t(row0) * d * 2;
-        CUtensorMap tmH_k, tmH_mn, tmY_st, tmDz_k, tmDz_mn, tmPart;
+        CUtensorMap tmH_k, tmH_mn, tmHT_k, tmY_st, tmDz_k, tmDz_mn, tmPart;
         FKL_TMAP(tmH_k, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 128);
         FKL_TMAP(tmH_mn, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 64);
-        FKL_TMAP(tmY_st, F16, yz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 32);
-        FKL_TMAP(tmDz_k, BF16, yz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 128);
-        FKL_TMAP(tmDz_mn, BF16, yz, uint64_t(V), uint64_t(rows), uint64_t(P.Vs) * 2, 64, 64);
+        // the dW GEMM's B operand: each CTA of a pair loads half of a (sub-)tile's columns of d
+        FKL_TMAP(tmHT_k, BF16, hT, uint64_t(rows), uint64_t(d), uint64_t(P.Cc) * 2, 64,
+                 uint32_t(std::min(P.bn_dw, 256) / 2));
+        FKL_PANEL_TMAP(tmY_st, F16, yz, 32);
+        FKL_PANEL_TMAP(tmDz_k, BF16, yz, 128);
+        FKL_PANEL_TMAP(tmDz_mn, BF16, yz, 64);
         FKL_TMAP(tmPart, F32, part, uint64_t(d), uint64_t(P.splits) * P.Cc, uint64_t(d) * 4, 32, 32);
+        FKL_SMALL(KK_TRANSPOSE_H, launch_transpose_h(hc, rows, d, hT, P.Cc, s));
 
         // logits of the chunk: lse / gather partials, and y = z log2e/T - tile max kept in fp16
         GemmParams p{};
@@ -857,9 +922,9 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
         FKL_SMALL(KK_FWD_FINALIZE,
                   launch_fwd_finalize(pm, pl, pg, P.Cc, P.nt_v, rows, H, valid, T, lse + row0, rowloss + row0, s));
         // dz from the kept logits, in place (no second pass over the tensor cores)
-        FKL_SMALL(KK_FB_DZ, launch_dz_from_logits(yz, P.Vs, V, pm, P.Cc, lse + row0, valid, n_valid, grad_loss, T,
+        FKL_SMALL(KK_FB_DZ, launch_dz_from_logits(yz, int64_t(P.Cc) * 64, V, pm, P.Cc, lse + row0, valid, n_valid, grad_loss, T,
                                                   sidx, sp, K, rows, s));
-        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmH_mn, tmW_mn, tmPart, tmDW, part,
+        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmHT_k, tmH_mn, tmW_mn, tmPart, tmDW, part,
                                           static_cast<char*>(dh) + size_t(row0) * d * 2, status, s))
             return st;
     }
@@ -927,10 +992,11 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
         p.K = K;
         FKL_CUDA_TRY(cudaMemsetAsync(any_flag, 0, sizeof(int), s));
         if (fkl_status st = run_gemm(KK_TK_GEMM_TMAX, 256, 0, 0, EPI_TMAX, tmH, tmW, tmW, p, flop, s)) return st;
-        FKL_SMALL(KK_TK_THRESHOLD, launch_topk_threshold(part, P.Cc, P.nt_v, rows, K, theta, cnt_gt, cnt_eq, s));
-        FKL_SMALL(KK_TK_GATHER, launch_topk_gather(part, top_v, top_i, P.Cc, P.nt_v, rows, K, theta, cnt_gt, cnt_eq,
-                                                   cand_v, cand_i, P.cap, tie_i, row_flag, any_flag, s));
-        // the second tensor-core pass, for the rows the gather flagged; it returns at once if none is
+        // theta, candidates and selection per row; rows it cannot complete are flagged
+        FKL_SMALL(KK_TK_ROWS, launch_topk_rows(part, top_v, top_i, P.Cc, P.nt_v, rows, K, theta, cnt_gt, cnt_eq,
+                                               row_flag, any_flag, idx + size_t(row0) * K, logit + size_t(row0) * K,
+                                               s));
+        // the second tensor-core pass, for the flagged rows; it returns at once if none is
         p.any_flag = any_flag;
         p.row_flag = row_flag;
         p.theta = theta;
@@ -942,8 +1008,8 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
         p.tie_i = tie_i;
         // (its FLOP are not counted: the launch usually returns at once)
         if (fkl_status st = run_gemm(KK_TK_GEMM_CAND, 256, 0, 0, EPI_CAND, tmH, tmW, tmW, p, 0.0, s)) return st;
-        FKL_SMALL(KK_TK_SELECT, launch_topk_select(cand_v, cand_i, P.cap, cnt_gt, cnt_eq, tie_i, theta, rows, K,
-                                                   idx + size_t(row0) * K, logit + size_t(row0) * K, s));
+        FKL_SMALL(KK_TK_SELECT, launch_topk_select(cand_v, cand_i, P.cap, cnt_gt, cnt_eq, tie_i, theta, row_flag, rows,
+                                                   K, idx + size_t(row0) * K, logit + size_t(row0) * K, s));
     }
     return FKL_OK;
 }

@@ -34,12 +34,12 @@ enum KernelKind {
     KK_FB_GEMM_LSE_Y,  // tcgen05 GEMM z = h W^T, logsumexp / gather epilogue that also keeps the logits
     KK_FB_DZ,          // dz from the kept logits (elementwise)
     KK_TK_GEMM_TMAX,   // teacher top-K: tcgen05 GEMM, per-row max of each vocabulary tile
-    KK_TK_THRESHOLD,   // teacher top-K: per-row K-th largest tile max
+    KK_TK_ROWS,        // teacher top-K: per-row threshold, candidates and selection (one warp per row)
     KK_TK_GEMM_CAND,   // teacher top-K: tcgen05 GEMM again for flagged rows (returns at once if none)
-    KK_TK_SELECT,      // teacher top-K: per-row selection and sort of the candidates
+    KK_TK_SELECT,      // teacher top-K: selection for the rows the second tensor-core pass completed
     KK_SELFTEST_WAIT,  // bounded-wait self-test
     KK_SCALE_GRADS,    // dh, dW times an upstream gradient
-    KK_TK_GATHER,      // teacher top-K: candidates from the per-tile top four
+    KK_TRANSPOSE_H,    // h of a chunk transposed: the dW GEMM's K-major operand
     KK_NUM
 };
 
@@ -62,6 +62,7 @@ constexpr bool epi_staged(int epi) {
 struct GemmParams {
     int m_tiles, n_tiles, splits, kb_total, m_fastest;
     int M;             // valid rows of the output (rows beyond are not written)
+    int a_panel;       // 1: A is the dz panel buffer, a 3-D map {64 columns, rows, panel}
     int Ncols;         // valid columns (V for the logit GEMMs, d for dh / dW)
     int* status;       // device status word
     // EPI_LSE / EPI_DZ
@@ -129,17 +130,16 @@ void launch_loss_reduce(const float* rowloss, int64_t N, const int* n_valid, flo
                         cudaStream_t s);
 void launch_dh_reduce(const float* part, int splits, size_t split_elems, int rows, int d, void* dh,
                       cudaStream_t s);
-void launch_topk_threshold(const float* part_m, int part_stride, int ntiles, int rows, int K, float* theta,
-                           int* cnt_gt, int* cnt_eq, cudaStream_t s);
-void launch_topk_gather(const float* part_m, const float* top_v, const int* top_i, int part_stride, int ntiles,
-                        int rows, int K, const float* theta, int* cnt_gt, int* cnt_eq, float* cand_v, int* cand_i,
-                        int cap, int* tie_i, uint8_t* row_flag, int* any_flag, cudaStream_t s);
+void launch_topk_rows(const float* part_m, const float* top_v, const int* top_i, int part_stride, int ntiles,
+                      int rows, int K, float* theta, int* cnt_gt, int* cnt_eq, uint8_t* row_flag, int* any_flag,
+                      int32_t* idx_out, float* logit_out, cudaStream_t s);
 void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const int* cnt_gt, const int* cnt_eq,
-                        const int* tie_i, const float* theta, int rows, int K, int32_t* idx_out, float* logit_out,
-                        cudaStream_t s);
+                        const int* tie_i, const float* theta, const uint8_t* row_flag, int rows, int K,
+                        int32_t* idx_out, float* logit_out, cudaStream_t s);
 void launch_scale_grads(void* dh, size_t n_dh, float* dW, size_t n_dw, const float* g, int grid, cudaStream_t s);
-void launch_dz_from_logits(void* yz, int64_t Vs, int64_t V, const float* part_m, int part_stride,
+void launch_dz_from_logits(void* yz, int64_t pstride, int64_t V, const float* part_m, int part_stride,
                            const float* lse, const uint8_t* valid, const int* n_valid, const float* grad,
                            float T, const int* sidx, const float* sp, int K, int rows, cudaStream_t s);
+void launch_transpose_h(const void* h, int rows, int d, void* hT, int64_t ld, cudaStream_t s);
 
 }  // namespace fkl

@@ -254,7 +254,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t fb = full_leader + 8u * stage;
                     if (leader) mbar_arrive_expect_tx(full0 + 8u * stage, 2u * C::STAGE_BYTES);
                     if (A_MN == 0) {
-                        tma_load_2d_pair(sa, &tmA, fb, kb * kBK, arow);
+                        if (p.a_panel) tma_load_3d_pair(sa, &tmA, fb, 0, arow, kb);
+                        else tma_load_2d_pair(sa, &tmA, fb, kb * kBK, arow);
+                    } else if (p.a_panel) {  // the CTA's 128 A rows are two 64-column panels
+                        tma_load_3d_pair(sa, &tmA, fb, 0, kb * kBK, arow >> 6);
+                        tma_load_3d_pair(sa + 8192u, &tmA, fb, 0, kb * kBK, (arow >> 6) + 1);
                     } else {
                         tma_load_2d_pair(sa, &tmA, fb, arow, kb * kBK);
                         tma_load_2d_pair(sa + 8192u, &tmA, fb, arow + 64, kb * kBK);
@@ -570,7 +574,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0 && wrow < p.M) {
-                        tma_store_2d(&tmOut, buf, col0, wrow);
+                        tma_store_3d(&tmOut, buf, 0, wrow, col0 >> 6);
                         bulk_commit();
                     }
                     ++box;
@@ -746,7 +750,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0 && wrow < p.M) {
-                        tma_store_2d(&tmOut, buf, col0, wrow);
+                        tma_store_3d(&tmOut, buf, 0, wrow, col0 >> 6);
                         bulk_commit();
                     }
                     ++box;

@@ -102,10 +102,17 @@ def test_scale_grads_rejects(L, args):
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(L):
+    # 2^24 rows: the 4 bytes per row alone exceed the scratch, so no chunk fits and N is named
     st = L.fkl_forward_noalloc(A16, A16, A16, A16, None, 1 << 24, 2880, 201088, 100, 1.0, 0,
                                A16, A16, None, None)
     assert st == WORKSPACE
-    assert b"scratch" in L.fkl_last_error()
+    msg = L.fkl_last_error()
+    assert b"scratch" in msg and b"smallest chunk" in msg and b"fewer rows" in msg
+    # a size that fits at a smaller chunk: the message asks for one
+    st = L.fkl_forward_noalloc(A16, A16, A16, A16, None, 32768, 2880, 201088, 100, 1.0, 8192,
+                               A16, A16, None, None)
+    assert st == WORKSPACE
+    assert b"smaller chunk" in L.fkl_last_error()
     # and the usual argument checks come first
     st = L.fkl_forward_noalloc(A16, A16, A16, A16, None, 10, 60, 100, 4, 1.0, 0, A16, A16, None, None)
     assert st == INVALID

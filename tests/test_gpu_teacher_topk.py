@@ -157,3 +157,19 @@ def test_spread_top_logits_need_one_pass():
     idx, val, second = _run_ws(x["h"][:1024], x["W"], 100)
     assert second == 0
     _check(x["h"][:1024], x["W"], 100, idx, val, rows=np.arange(0, 1024, 64))
+
+
+def test_mixed_one_and_two_pass_rows():
+    """Every other row carries the clustered top logits (second pass); the rows in
+    between complete in the first pass.  Both kinds share a chunk, and each must
+    come out exact: the second pass's selection touches only the flagged rows."""
+    rng = np.random.default_rng(7600)
+    N, d, V, K = 300, 64, 6000, 32
+    hf = rng.standard_normal((N, d))
+    hf[::2, 0] = 4.0
+    Wf = rng.standard_normal((V, d)) / np.sqrt(d)
+    Wf[10:22, 0] = 2.5 + 0.05 * np.arange(12)
+    h, W = _bf16(hf), _bf16(Wf)
+    idx, val, second = _run_ws(h, W, K)
+    assert second == 1
+    _check(h, W, K, idx, val)

@@ -7,10 +7,12 @@ and can fail under memory pressure.  For them the library carries a fixed
 64 MiB scratch array of its own; the caller passes only inputs and outputs.
 
 Checked here through the C ABI: two calls in a row (different sizes, so the
-second one runs over the first one's leftovers in the shared scratch) agree with
-fkl_forward on a caller workspace within the parity tolerances; a teacher id
-outside [0, V) is reported through the status output; a size whose scratch would
-exceed the array is refused on the host before any launch.
+second one runs over the first one's leftovers in the shared scratch) give
+bit for bit the loss and lse of fkl_forward on a caller workspace (the same
+kernels in the same order), and the first of them matches the fp64 oracle
+within the parity tolerances; a teacher id outside [0, V) is reported through
+the status output; a size whose scratch would exceed the array is refused on the
+host before any launch.
 
 This file is collected last on purpose (its name sorts after every other test).
 """
@@ -20,8 +22,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from lm_head_kl_fkl_b300 import _lib, api, synth
-from tests.gpu_helpers import TOL_LOSS_REL, TOL_LSE_ABS, to_device
+from tests.gpu_helpers import TOL_LOSS_REL, TOL_LSE_ABS, oracle_inputs, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -54,9 +57,17 @@ def _check_against_workspace_forward(xd, chunk, out):
     assert dstat == 0
     ref_loss, ref_lse = api.forward(xd["h"], xd["W"], xd["idx"], xd["t"], xd["mask"], xd["T"], chunk)
     torch.cuda.synchronize()
-    rl = float(ref_loss.item())
-    assert abs(float(loss.item()) - rl) <= TOL_LOSS_REL * abs(rl), (float(loss.item()), rl)
-    err = float((lse - ref_lse).abs().max().item())
+    # the same launch sequence on the same inputs: bit-identical results
+    assert float(loss.item()) == float(ref_loss.item()), (float(loss.item()), float(ref_loss.item()))
+    assert torch.equal(lse, ref_lse), float((lse - ref_lse).abs().max().item())
+
+
+def _check_against_oracle(x, out):
+    _, loss, lse, _ = out
+    h, W = oracle_inputs(x)
+    ref = oracle.forward(h, W, x["idx"], x["t"], x["mask"], x["T"])
+    assert abs(float(loss.item()) - ref["loss"]) <= TOL_LOSS_REL * abs(ref["loss"]), (float(loss.item()), ref["loss"])
+    err = float(np.abs(lse.cpu().numpy().astype(np.float64) - ref["lse"]).max())
     assert err <= TOL_LSE_ABS, err
 
 
@@ -64,7 +75,9 @@ def test_two_calls_match_workspace_forward():
     # first call: several chunks and vocabulary tiles, ragged everywhere
     xa = synth.make_inputs(700, 136, 3001, 24, 1.5, 0.05, "uniform", seed=4242)
     da = to_device(xa)
-    _check_against_workspace_forward(da, 256, _noalloc(da, chunk=256))
+    out_a = _noalloc(da, chunk=256)
+    _check_against_workspace_forward(da, 256, out_a)
+    _check_against_oracle(xa, out_a)
     # second call, straight after: other sizes and the default chunk, over the
     # scratch contents the first call left behind
     xb = synth.make_inputs(1300, 256, 5000, 100, 1.0, 0.05, "zipf1.1", seed=4243)
@@ -96,3 +109,4 @@ def test_oversized_request_refused_before_launch():
     msg = _lib.lib().fkl_last_error().decode()
     assert "scratch" in msg and str(SCRATCH_BYTES) in msg
     assert api.launch_count() == before
+
