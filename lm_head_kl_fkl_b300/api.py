@@ -56,6 +56,30 @@ def _expect(t, name, dtype, ndim, device=None):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _expect_out(t, name, dtype, shape, device):
+    """A caller-supplied output: its dtype, shape, device and layout as the library writes it."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    _expect(t, name, dtype, len(shape), device)
+
+
+def _ws_bytes(ws, device) -> int:
+    """Byte size of a caller-supplied workspace (any dtype), which must be contiguous device memory on h's device."""
+    if not isinstance(ws, torch.Tensor):
+        raise TypeError("ws must be a torch.Tensor")
+    if not ws.is_cuda:
+        raise ValueError("ws must be a CUDA tensor")
+    if ws.device != device:
+        raise ValueError(f"ws is on {ws.device}, expected {device}")
+    if not ws.is_contiguous():
+        raise ValueError("ws must be contiguous")
+    return ws.numel() * ws.element_size()
+
+
 def workspace_size(N: int, d: int, V: int, K: int, chunk: int = 0) -> int:
     n = _lib.lib().fkl_workspace_size(int(N), int(d), int(V), int(K), int(chunk))
     if n == 0:
@@ -86,6 +110,27 @@ def _inputs(h, W, idx, tlogit, mask):
     return N, d, V, idx.shape[1], dev
 
 
+def _grad_scalar(g, device):
+    """The upstream gradient as the library reads it: one fp32 value in device memory (or None = 1)."""
+    if g is None:
+        return None
+    if not isinstance(g, torch.Tensor) or g.numel() != 1:
+        raise ValueError("grad_loss must be a one-element tensor")
+    g = g.reshape(1)
+    _expect(g, "grad_loss", torch.float32, 1, device)
+    return g
+
+
+def _grad_outputs(dh, dW, N, d, V, device):
+    if dh is None:
+        dh = torch.empty((N, d), dtype=torch.bfloat16, device=device)
+    _expect_out(dh, "dh", torch.bfloat16, (N, d), device)
+    if dW is None:
+        dW = torch.empty((V, d), dtype=torch.float32, device=device)
+    _expect_out(dW, "dW", torch.float32, (V, d), device)
+    return dh, dW
+
+
 def forward(h, W, idx, tlogit, mask=None, T: float = 1.0, chunk: int = 0,
             ws: Optional[torch.Tensor] = None, loss: Optional[torch.Tensor] = None,
             lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
@@ -93,10 +138,15 @@ def forward(h, W, idx, tlogit, mask=None, T: float = 1.0, chunk: int = 0,
     N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
     if ws is None:
         ws = alloc_workspace(N, d, V, K, chunk, dev)
-    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
-    lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
+    ws_bytes = _ws_bytes(ws, dev)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    _expect_out(loss, "loss", torch.float32, (1,), dev)
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    _expect_out(lse, "lse", torch.float32, (N,), dev)
     st = _lib.lib().fkl_forward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
-                                float(T), int(chunk), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
+                                float(T), int(chunk), _ptr(loss), _ptr(lse), _ptr(ws), ws_bytes,
                                 _stream(dev))
     _check(st, "fkl_forward")
     return loss, lse
@@ -108,16 +158,15 @@ def backward(h, W, idx, tlogit, mask, T: float, lse: torch.Tensor,
              dW: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Fused backward: returns (dh [N,d] bf16, dW [V,d] fp32)."""
     N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
-    _expect(lse, "lse", torch.float32, 1, dev)
-    if grad_loss is not None:
-        _expect(grad_loss.reshape(-1), "grad_loss", torch.float32, 1, dev)
+    _expect_out(lse, "lse", torch.float32, (N,), dev)
+    grad_loss = _grad_scalar(grad_loss, dev)
     if ws is None:
         ws = alloc_workspace(N, d, V, K, chunk, dev)
-    dh = torch.empty((N, d), dtype=torch.bfloat16, device=dev) if dh is None else dh
-    dW = torch.empty((V, d), dtype=torch.float32, device=dev) if dW is None else dW
+    ws_bytes = _ws_bytes(ws, dev)
+    dh, dW = _grad_outputs(dh, dW, N, d, V, dev)
     st = _lib.lib().fkl_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
                                  float(T), int(chunk), _ptr(lse), _ptr(grad_loss), _ptr(dh),
-                                 _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
+                                 _ptr(dW), _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "fkl_backward")
     return dh, dW
 
@@ -126,15 +175,16 @@ def mix_forward(h, W, idx, tlogit, mask, label, T: float, alpha: float, chunk: i
                 ws: Optional[torch.Tensor] = None):
     """KL + hard-label CE mixture, forward: (loss [1], lse [N], lse1 [N]) fp32."""
     N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
-    _expect(label, "label", torch.int32, 1, dev)
+    _expect_out(label, "label", torch.int32, (N,), dev)
     if ws is None:
         ws = alloc_workspace(N, d, V, K, chunk, dev)
+    ws_bytes = _ws_bytes(ws, dev)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     lse1 = torch.empty(N, dtype=torch.float32, device=dev)
     st = _lib.lib().fkl_mix_forward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), _ptr(label), N, d, V,
                                     K, float(T), float(alpha), int(chunk), _ptr(loss), _ptr(lse), _ptr(lse1),
-                                    _ptr(ws), ws.numel(), _stream(dev))
+                                    _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "fkl_mix_forward")
     return loss, lse, lse1
 
@@ -143,18 +193,17 @@ def mix_backward(h, W, idx, tlogit, mask, label, T: float, alpha: float, lse, ls
                  grad_loss: Optional[torch.Tensor] = None, chunk: int = 0, ws: Optional[torch.Tensor] = None):
     """KL + hard-label CE mixture, backward: (dh [N,d] bf16, dW [V,d] fp32)."""
     N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
-    _expect(label, "label", torch.int32, 1, dev)
-    _expect(lse, "lse", torch.float32, 1, dev)
-    _expect(lse1, "lse1", torch.float32, 1, dev)
-    if grad_loss is not None:
-        _expect(grad_loss.reshape(-1), "grad_loss", torch.float32, 1, dev)
+    _expect_out(label, "label", torch.int32, (N,), dev)
+    _expect_out(lse, "lse", torch.float32, (N,), dev)
+    _expect_out(lse1, "lse1", torch.float32, (N,), dev)
+    grad_loss = _grad_scalar(grad_loss, dev)
     if ws is None:
         ws = alloc_workspace(N, d, V, K, chunk, dev)
-    dh = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
-    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    ws_bytes = _ws_bytes(ws, dev)
+    dh, dW = _grad_outputs(None, None, N, d, V, dev)
     st = _lib.lib().fkl_mix_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), _ptr(label), N, d,
                                      V, K, float(T), float(alpha), int(chunk), _ptr(lse), _ptr(lse1),
-                                     _ptr(grad_loss), _ptr(dh), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
+                                     _ptr(grad_loss), _ptr(dh), _ptr(dW), _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "fkl_mix_backward")
     return dh, dW
 
@@ -167,17 +216,20 @@ def forward_backward(h, W, idx, tlogit, mask, T: float, grad_loss: Optional[torc
 
     Returns (loss [1] fp32, lse [N] fp32, dh [N,d] bf16, dW [V,d] fp32)."""
     N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
-    if grad_loss is not None:
-        _expect(grad_loss.reshape(-1), "grad_loss", torch.float32, 1, dev)
+    grad_loss = _grad_scalar(grad_loss, dev)
     if ws is None:
         ws = alloc_workspace(N, d, V, K, chunk, dev)
-    loss = torch.empty(1, dtype=torch.float32, device=dev) if loss is None else loss
-    lse = torch.empty(N, dtype=torch.float32, device=dev) if lse is None else lse
-    dh = torch.empty((N, d), dtype=torch.bfloat16, device=dev) if dh is None else dh
-    dW = torch.empty((V, d), dtype=torch.float32, device=dev) if dW is None else dW
+    ws_bytes = _ws_bytes(ws, dev)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    _expect_out(loss, "loss", torch.float32, (1,), dev)
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    _expect_out(lse, "lse", torch.float32, (N,), dev)
+    dh, dW = _grad_outputs(dh, dW, N, d, V, dev)
     st = _lib.lib().fkl_forward_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
                                          float(T), int(chunk), _ptr(grad_loss), _ptr(loss), _ptr(lse),
-                                         _ptr(dh), _ptr(dW), _ptr(ws), ws.numel(), _stream(dev))
+                                         _ptr(dh), _ptr(dW), _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "fkl_forward_backward")
     return loss, lse, dh, dW
 
@@ -202,10 +254,11 @@ def teacher_topk(h: torch.Tensor, W: torch.Tensor, K: int, chunk: int = 0,
     L = _lib.lib()
     if ws is None:
         ws = torch.empty(topk_workspace_size(N, d, V, K, chunk), dtype=torch.uint8, device=dev)
+    ws_bytes = _ws_bytes(ws, dev)
     idx = torch.empty((N, K), dtype=torch.int32, device=dev)
     logit = torch.empty((N, K), dtype=torch.float32, device=dev)
     st = L.fkl_teacher_topk(_ptr(h), _ptr(W), N, d, V, int(K), int(chunk), _ptr(idx), _ptr(logit), _ptr(ws),
-                            ws.numel(), _stream(dev))
+                            ws_bytes, _stream(dev))
     _check(st, "fkl_teacher_topk")
     return idx, logit
 
@@ -215,16 +268,25 @@ def get_status(ws: torch.Tensor) -> int:
     return int(_lib.lib().fkl_get_status(_ptr(ws), _stream(ws.device)))
 
 
+def _raise_on_device_status(ws: torch.Tensor, where: str):
+    """Reads the workspace's device status word (synchronising the stream) and raises on an error."""
+    st = get_status(ws)
+    if st != 0:
+        raise FKLError(st, f"{where} (device status)")
+
+
 class FKLLoss(torch.autograd.Function):
     """T^2 * mean over valid rows of KL(p_teacher || q_student); gradients for h and W."""
 
     @staticmethod
-    def forward(ctx, h, W, idx, tlogit, mask, T, chunk):
+    def forward(ctx, h, W, idx, tlogit, mask, T, chunk, check_status=False):
         N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
         ws = alloc_workspace(N, d, V, K, chunk, dev)
         loss, lse = forward(h, W, idx, tlogit, mask, T, chunk, ws=ws)
+        if check_status:
+            _raise_on_device_status(ws, "fkl_forward")
         ctx.save_for_backward(h, W, idx, tlogit, lse)
-        ctx.mask, ctx.T, ctx.chunk, ctx.ws = mask, T, chunk, ws
+        ctx.mask, ctx.T, ctx.chunk, ctx.ws, ctx.check_status = mask, T, chunk, ws, check_status
         return loss.reshape(())
 
     @staticmethod
@@ -233,8 +295,10 @@ class FKLLoss(torch.autograd.Function):
         g = g.reshape(1).to(torch.float32).contiguous()
         dh, dW = backward(h, W, idx, tlogit, ctx.mask, ctx.T, lse, grad_loss=g, chunk=ctx.chunk,
                           ws=ctx.ws)
+        if ctx.check_status:
+            _raise_on_device_status(ctx.ws, "fkl_backward")
         ctx.ws = None
-        return dh, dW.to(W.dtype), None, None, None, None, None
+        return dh, dW.to(W.dtype), None, None, None, None, None, None
 
 
 class FKLLossKeepLogits(torch.autograd.Function):
@@ -244,8 +308,12 @@ class FKLLossKeepLogits(torch.autograd.Function):
     dW are allocated in the forward and held until the backward."""
 
     @staticmethod
-    def forward(ctx, h, W, idx, tlogit, mask, T, chunk):
-        loss, _, dh, dW = forward_backward(h, W, idx, tlogit, mask, T, chunk=chunk)
+    def forward(ctx, h, W, idx, tlogit, mask, T, chunk, check_status=False):
+        N, d, V, K, dev = _inputs(h, W, idx, tlogit, mask)
+        ws = alloc_workspace(N, d, V, K, chunk, dev)
+        loss, _, dh, dW = forward_backward(h, W, idx, tlogit, mask, T, chunk=chunk, ws=ws)
+        if check_status:
+            _raise_on_device_status(ws, "fkl_forward_backward")
         ctx.save_for_backward(dh, dW)
         ctx.w_dtype = W.dtype
         return loss.reshape(())
@@ -257,19 +325,25 @@ class FKLLossKeepLogits(torch.autograd.Function):
         N, d = dh.shape
         st = _lib.lib().fkl_scale_grads(_ptr(dh), _ptr(dW), N, d, dW.shape[0], _ptr(g), _stream(dh.device))
         _check(st, "fkl_scale_grads")
-        return dh, dW.to(ctx.w_dtype), None, None, None, None, None
+        return dh, dW.to(ctx.w_dtype), None, None, None, None, None, None
 
 
 def fkl_loss(h, W, idx, tlogit, mask=None, T: float = 1.0, chunk: int = 0,
-             keep_logits: bool = False) -> torch.Tensor:
+             keep_logits: bool = False, check_status: bool = False) -> torch.Tensor:
     """Autograd-aware fused loss (scalar).
 
     keep_logits=False: fkl_forward now, fkl_backward (logits recomputed) in autograd's
     backward.  keep_logits=True: loss and gradients together in the forward, without
-    the recompute; faster, with dh and dW held from the forward to the backward."""
+    the recompute; faster, with dh and dW held from the forward to the backward.
+
+    Errors found on the device (a teacher id outside [0, V), a pipeline wait that
+    timed out) only set the workspace's status word; the loss and the gradients are
+    then undefined.  check_status=True reads that word after each library pass (one
+    stream synchronisation each) and raises FKLError on an error; with the default
+    False the caller is responsible for validating the teacher ids."""
     if keep_logits:
-        return FKLLossKeepLogits.apply(h, W, idx, tlogit, mask, T, chunk)
-    return FKLLoss.apply(h, W, idx, tlogit, mask, T, chunk)
+        return FKLLossKeepLogits.apply(h, W, idx, tlogit, mask, T, chunk, check_status)
+    return FKLLoss.apply(h, W, idx, tlogit, mask, T, chunk, check_status)
 
 
 # ---- measurement hooks -------------------------------------------------------
