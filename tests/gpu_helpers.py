@@ -39,3 +39,11 @@ def rel_l2(a, b):
 
 def oracle_inputs(x):
     return synth.bf16_bits_to_f64(x["h"]), synth.bf16_bits_to_f64(x["W"])
+
+
+def both_oracles():
+    """[(name, oracle)] for the two independent fp64 oracles: the plain C++ one (one
+    full logit row at a time, loops only) and the numpy one (a library matmul)."""
+    import oracle
+    from oracle import cpp
+    return [("cpp", cpp.load()), ("numpy", oracle)]

@@ -6,8 +6,8 @@ import torch
 
 import oracle
 from lm_head_kl_fkl_b300 import api, synth
-from tests.gpu_helpers import (TOL_GRAD_REL_L2, TOL_LOSS_REL, TOL_LSE_ABS, oracle_inputs, rel_l2,
-                               run_fused, to_device)
+from tests.gpu_helpers import (TOL_GRAD_REL_L2, TOL_LOSS_REL, TOL_LSE_ABS, both_oracles, oracle_inputs,
+                               rel_l2, run_fused, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,15 +29,17 @@ def _run_mix(xd, label, alpha, chunk=0, grad=None):
                 dW=dW.cpu().numpy().astype(np.float64))
 
 
-def _check(x, label, alpha, out, grad=1.0):
+def _check(x, label, alpha, out, grad=1.0, oracles=None):
+    """Against the plain C++ and the numpy fp64 oracles (or the ones given)."""
     h, W = oracle_inputs(x)
-    ref = oracle.forward_mix(h, W, x["idx"], x["t"], x["mask"], label, x["T"], alpha)
-    g = oracle.backward_mix(h, W, x["idx"], x["t"], x["mask"], label, x["T"], alpha, grad_loss=grad)
-    assert abs(out["loss"] - ref["loss"]) <= TOL_LOSS_REL * abs(ref["loss"]), (out["loss"], ref["loss"])
-    assert np.abs(out["lse"] - ref["lse"]).max() <= TOL_LSE_ABS
-    assert np.abs(out["lse1"] - ref["lse1"]).max() <= TOL_LSE_ABS
-    assert rel_l2(out["dh"], g["dh"]) <= TOL_GRAD_REL_L2, rel_l2(out["dh"], g["dh"])
-    assert rel_l2(out["dW"], g["dW"]) <= TOL_GRAD_REL_L2, rel_l2(out["dW"], g["dW"])
+    for name, orc in (oracles or both_oracles()):
+        ref = orc.forward_mix(h, W, x["idx"], x["t"], x["mask"], label, x["T"], alpha)
+        g = orc.backward_mix(h, W, x["idx"], x["t"], x["mask"], label, x["T"], alpha, grad_loss=grad)
+        assert abs(out["loss"] - ref["loss"]) <= TOL_LOSS_REL * abs(ref["loss"]), (name, out["loss"], ref["loss"])
+        assert np.abs(out["lse"] - ref["lse"]).max() <= TOL_LSE_ABS, name
+        assert np.abs(out["lse1"] - ref["lse1"]).max() <= TOL_LSE_ABS, name
+        assert rel_l2(out["dh"], g["dh"]) <= TOL_GRAD_REL_L2, (name, rel_l2(out["dh"], g["dh"]))
+        assert rel_l2(out["dW"], g["dW"]) <= TOL_GRAD_REL_L2, (name, rel_l2(out["dW"], g["dW"]))
 
 
 CASES = [
@@ -82,4 +84,4 @@ def test_small_lm_head_workload():
     """The small LM head workload (N=4096, d=2048, V=32768, K=100, T=2) at full size."""
     x = synth.config_inputs(1)
     label = _labels(x, 8400)
-    _check(x, label, 0.5, _run_mix(to_device(x), label, 0.5))
+    _check(x, label, 0.5, _run_mix(to_device(x), label, 0.5), oracles=[("numpy", oracle)])

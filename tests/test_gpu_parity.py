@@ -1,33 +1,35 @@
-"""Fused CUDA path against the fp64 oracle, element by element, on sizes the
-oracle finishes in seconds (several tiles, ragged tails in N, d and V, several
-chunks), plus edge cases."""
+"""Fused CUDA path against the fp64 oracles, element by element, on sizes the
+oracles finish in seconds (several tiles, ragged tails in N, d and V, several
+chunks), plus edge cases.  Every case is compared with both independent oracles:
+the plain C++ one (loops, one full logit row per token) and the numpy one."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from lm_head_kl_fkl_b300 import api, synth
-from tests.gpu_helpers import (TOL_GRAD_REL_L2, TOL_LOSS_REL, TOL_LSE_ABS, oracle_inputs, rel_l2,
-                               run_fused, to_device)
+from tests.gpu_helpers import (TOL_GRAD_REL_L2, TOL_LOSS_REL, TOL_LSE_ABS, both_oracles, oracle_inputs,
+                               rel_l2, run_fused, to_device)
 
 pytestmark = pytest.mark.gpu
 
 
 def _check(x, out, grad=1.0, tol_scale=1.0):
+    """The GPU result against each of the two fp64 oracles (plain C++ and numpy)."""
     h, W = oracle_inputs(x)
-    ref = oracle.forward(h, W, x["idx"], x["t"], x["mask"], x["T"])
-    g = oracle.backward(h, W, x["idx"], x["t"], x["mask"], x["T"], grad_loss=grad)
-    if ref["n_valid"] > 0:
-        assert abs(out["loss"] - ref["loss"]) <= TOL_LOSS_REL * abs(ref["loss"]), (out["loss"], ref["loss"])
-    else:
-        assert out["loss"] == 0.0
-    assert np.abs(out["lse"] - ref["lse"]).max() <= TOL_LSE_ABS
-    if ref["n_valid"] > 0:
-        assert rel_l2(out["dh"], g["dh"]) <= TOL_GRAD_REL_L2 * tol_scale, rel_l2(out["dh"], g["dh"])
-        assert rel_l2(out["dW"], g["dW"]) <= TOL_GRAD_REL_L2 * tol_scale, rel_l2(out["dW"], g["dW"])
-    else:
-        assert not out["dh"].any() and not out["dW"].any()
-    return ref, g
+    for name, orc in both_oracles():
+        ref = orc.forward(h, W, x["idx"], x["t"], x["mask"], x["T"])
+        g = orc.backward(h, W, x["idx"], x["t"], x["mask"], x["T"], grad_loss=grad)
+        if ref["n_valid"] > 0:
+            assert abs(out["loss"] - ref["loss"]) <= TOL_LOSS_REL * abs(ref["loss"]), (name, out["loss"], ref["loss"])
+        else:
+            assert out["loss"] == 0.0, name
+        assert np.abs(out["lse"] - ref["lse"]).max() <= TOL_LSE_ABS, name
+        if ref["n_valid"] > 0:
+            assert rel_l2(out["dh"], g["dh"]) <= TOL_GRAD_REL_L2 * tol_scale, (name, rel_l2(out["dh"], g["dh"]))
+            assert rel_l2(out["dW"], g["dW"]) <= TOL_GRAD_REL_L2 * tol_scale, (name, rel_l2(out["dW"], g["dW"]))
+        else:
+            assert not out["dh"].any() and not out["dW"].any(), name
 
 
 SHAPES = [
