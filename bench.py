@@ -35,9 +35,12 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM bytes (read + write) per launch of the dominant kernel at the default
-# gpt-oss-20b-like workload, from an ncu capture of a smaller case scaled by the
-# units processed, keyed by the kernel source digest they were taken on (see
-# profiles/dw_gemm_traffic.md); a stale digest gives null.
+# gpt-oss-20b-like workload: dram__bytes_read.sum + dram__bytes_write.sum from a
+# one-pass ncu capture of the same kernel on a two-chunk case with V = 32768,
+# averaged over its store and reduce-add launches as a full step mixes them and
+# scaled to V = 201088 by the vocabulary rows processed.  Keyed by the digest of
+# the kernel sources the capture ran; after any change of them the figure is
+# stale and the line reports null.
 TRAFFIC = {("bwd_gemm_dw", "fb0246ca0473"): 5.99e9}
 
 
@@ -256,6 +259,83 @@ def memory_stress(api, dev, stream, chunk, steps):
     return out
 
 
+def dominant_roofline(prof, peaks, peaks_kind):
+    """The tensor-core kernel with the largest share of the recorded time: its
+    algorithmic FLOP per launch over its mean CUDA-event launch time, against the
+    sustained measured bf16 peak (the kernels run inside a long power-capped step)."""
+    gemms = {k: v for k, v in prof.items() if v[2] > 0}
+    if not gemms:
+        return None
+    dom = max(gemms, key=lambda k: gemms[k][0])
+    tot_ms, n_l, fl = gemms[dom]
+    achieved = fl / (tot_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    return {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_kind": f"bf16 dense, sustained, {peaks_kind}",
+            "flop_per_launch": fl / n_l, "launch_ms": tot_ms / n_l, "launches": n_l}
+
+
+def kernel_table(prof):
+    total = max(1e-9, sum(p[0] for p in prof.values()))
+    return {k: {"ms_total": v[0], "launches": v[1], "share": v[0] / total,
+                **({"tflops": v[2] / (v[0] / 1e3) / 1e12} if v[2] > 0 else {})}
+            for k, v in prof.items()}
+
+
+def config_leg(api, cfg, dev, stream, chunk, steps, warmup, peaks, peaks_kind, with_cpu):
+    """fkl_forward + fkl_backward on another named workload (inputs resident in HBM):
+    time per step, tokens/s, TFLOP/s (8 N d V), the per-kernel list and its
+    dominant kernel's roofline, next to the C++ oracle on a bounded row sample."""
+    import torch
+    from lm_head_kl_fkl_b300 import synth
+    c = synth.CONFIGS[cfg]
+    x = synth.config_inputs(cfg)
+    N, d, V, K, T = c.N, c.d, c.V, c.K, c.T
+    h = torch.from_numpy(x["h"].view(np.int16)).view(torch.bfloat16).to(dev)
+    W = torch.from_numpy(x["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    idx, t, mask = (torch.from_numpy(x[k]).to(dev) for k in ("idx", "t", "mask"))
+    ws = api.alloc_workspace(N, d, V, K, chunk, dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dh = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+
+    def step():
+        api.forward(h, W, idx, t, mask, T, chunk, ws=ws, loss=loss, lse=lse)
+        api.backward(h, W, idx, t, mask, T, lse, chunk=chunk, ws=ws, dh=dh, dW=dW)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    api.profile_reset()
+    api.profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index or 0) as clk:
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    api.profile_enable(False)
+    prof = api.profile_read()
+    ms = e0.elapsed_time(e1) / steps
+    tflops = 8.0 * N * d * V / (ms / 1e3) / 1e12
+    out = {"workload": f"{c.name} fused top-K KL loss", "N": N, "d": d, "V": V, "K": K, "T": T,
+           "chunk": chunk or "default", "steps": steps, "warmup": warmup, "ms_per_step": ms,
+           "value": N / (ms / 1e3), "unit": "tokens/s", "tflops": tflops,
+           "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
+                                 "sustained": tflops / peaks["bf16_tflops_sustained"], "kind": peaks_kind},
+           "roofline": dominant_roofline(prof, peaks, peaks_kind), "kernels": kernel_table(prof),
+           "clocks": clk.summary(), "device_status": api.get_status(ws),
+           "l2": "inputs resident; W (V x d bf16) is larger than L2 at this size" if V * d * 2 > 126e6 else
+                 "inputs resident; the per-step working set exceeds L2 (dz and dW alone)"}
+    del h, W, idx, t, mask, ws, loss, lse, dh, dW
+    torch.cuda.empty_cache()
+    if with_cpu:
+        out["cpu_baseline"] = cpu_baseline(x, budget_s=6.0)
+    return out
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -358,23 +438,11 @@ def run_fused(args):
     tflops = flop_step / (ms_per_step / 1e3) / 1e12
 
     peaks, peaks_kind = load_peaks()
-    gemms = {k: v for k, v in prof.items() if v[2] > 0}
-    dom = max(gemms, key=lambda k: gemms[k][0]) if gemms else None
-    roofline = None
-    if dom:
-        tot_ms, n_l, fl = gemms[dom]
-        achieved = fl / (tot_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        dig = kernel_digest()
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                    "unit": "TFLOP/s", "frac": achieved / peak,
-                    "traffic": TRAFFIC.get((dom, dig)) if args.config == 3 and args.shape is None and not args.chunk
-                    else None,
-                    "peak_kind": f"bf16 dense, sustained, {peaks_kind}",
-                    "flop_per_launch": fl / n_l, "launch_ms": tot_ms / n_l, "launches": n_l}
-    kernels = {k: {"ms_total": v[0], "launches": v[1], "share": v[0] / max(1e-9, sum(p[0] for p in prof.values())),
-                   **({"tflops": v[2] / (v[0] / 1e3) / 1e12} if v[2] > 0 else {})}
-               for k, v in prof.items()}
+    roofline = dominant_roofline(prof, peaks, peaks_kind)
+    if roofline:
+        roofline["traffic"] = (TRAFFIC.get((roofline["kernel"], kernel_digest()))
+                               if args.config == 3 and args.shape is None and not args.chunk else None)
+    kernels = kernel_table(prof)
 
     # ---- the same step through fkl_forward_backward (one call, logits kept per chunk)
     variants = None
@@ -518,6 +586,14 @@ def run_fused(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x)
 
+    # ---- the smaller workloads (small LM head, Llama-8B->3.2B-like head) on the same call pair
+    legs = {}
+    if not args.no_config_legs and args.config == 3 and args.shape is None and world == 1:
+        del x
+        for cfg in (1, 2):
+            legs[f"config_{cfg}"] = config_leg(api, cfg, dev, stream, args.chunk, args.steps, args.warmup, peaks,
+                                               peaks_kind, with_cpu=not args.no_cpu_baseline)
+
     # ---- the memory-stress workload (N = 131072): peak device memory of the same call pair
     mem = None
     ws_gb = ws.numel() / 1e9
@@ -542,7 +618,7 @@ def run_fused(args):
                 "workspace_gb": ws_gb,
                 "resident_gb": base_mem / 1e9,
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-                "variants": variants, "teacher_topk": topk, "memory_stress": mem,
+                "variants": variants, "teacher_topk": topk, "memory_stress": mem, **legs,
                 "clocks": clk.summary(), "gpu_launches": launches, "device_status": status,
                 "kernel_digest": kernel_digest()}
         print(json.dumps(line), flush=True)
@@ -564,6 +640,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the one-call forward+backward timing")
     ap.add_argument("--no-memory-stress", action="store_true", help="skip the N=131072 peak-memory leg")
+    ap.add_argument("--no-config-legs", action="store_true",
+                    help="skip the small LM head and Llama-like head workloads (config_1, config_2 keys)")
     ap.add_argument("--shape", type=lambda s: tuple(int(v) for v in s.split(",")), default=None,
                     help="N,d,V,K: a smaller case of the chosen workload (profiling captures)")
     args = ap.parse_args()
