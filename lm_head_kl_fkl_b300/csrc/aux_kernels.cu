@@ -367,80 +367,103 @@ __device__ __forceinline__ int warp_sum(int c) {
     return c;
 }
 
-// theta of row r (one warp): the K-th largest of its per-tile maxima, or -inf when
-// there are fewer than K tiles.  At least K logits of the row are >= theta (each of
-// the K tiles contributes its max), and every logit > theta lies in one of the < K
-// tiles whose max exceeds theta, so at most (K - 1) * 256 logits are above it.
-__device__ __forceinline__ float row_theta(const float* __restrict__ part_m, int stride, int ntiles, int r, int K,
-                                           int lane) {
-    if (ntiles < K) return -INFINITY;
-    // the row's tile maxima, lane-strided, in registers (up to 32 x kTh of them),
-    // the rest re-read from memory on each step of the search
-    constexpr int kTh = 32;
-    uint32_t key[kTh];
-#pragma unroll
-    for (int j = 0; j < kTh; ++j) {
-        const int n = lane + 32 * j;
-        key[j] = n < ntiles ? fkey(part_m[static_cast<size_t>(n) * stride + r]) : 0u;
-    }
-    uint32_t t = 0;  // largest key with at least K tile maxima at or above it
-    for (int b = 31; b >= 0; --b) {
-        const uint32_t cand = t | (1u << b);
-        int c = 0;
-#pragma unroll
-        for (int j = 0; j < kTh; ++j) c += key[j] >= cand;
-        for (int n = lane + 32 * kTh; n < ntiles; n += 32)
-            c += fkey(part_m[static_cast<size_t>(n) * stride + r]) >= cand;
-        if (warp_sum(c) >= K) t = cand;
-    }
-    return unkey(t);
-}
-
 // Teacher top-K of one row per warp, from the first tensor-core pass's per-tile
-// top eight: theta (as above), then the candidates -- every kept logit > theta of
-// the tiles whose max reaches theta, and up to K logits == theta -- compacted into
-// shared memory, then the K largest (ties at the K-th value by the smallest ids)
-// sorted by value descending, ids ascending, and written out.  A tile whose eighth
-// kept logit is still >= theta may hold more candidates than were kept; such a row
-// (or one with more than kTopCap candidates) is flagged instead -- theta stored,
-// its counters cleared, nothing written -- for the second tensor-core pass and
+// top eight (tile maxima part_m [tile][row], kept logits and ids [tile][row][8]):
+//  1. theta = the K-th largest of the row's tile maxima (-inf with fewer than K
+//     tiles), by a bitwise search over order-preserving keys held in registers.
+//     At least K logits of the row are >= theta (each of the K tiles contributes
+//     its max), and every logit > theta lies in one of the < K tiles whose max
+//     exceeds theta.
+//  2. The tiles whose max reaches theta, listed in shared memory from the same
+//     registers; their kept logits are read 32 tiles at a time, and every kept
+//     logit > theta and up to K logits == theta are compacted, in tile order,
+//     into shared memory.
+//  3. The K largest (ties at the K-th value by the smallest ids), sorted by value
+//     descending and id ascending, written out.
+// A tile whose eighth kept logit is still >= theta may hold more candidates than
+// were kept; such a row (or one with more than kTopCap candidates or kTopHits
+// tiles) is flagged instead -- theta stored, its counters cleared, its sub-chunk's
+// flag raised, nothing written -- for the second tensor-core pass and
 // topk_select_kernel.
-constexpr int kTopCap = 512;     // candidates > theta held in shared memory per row
-constexpr int kRowsPerBlock = 4;  // one warp per row
+constexpr int kRowsPerBlock = 8;  // one warp per row
+constexpr int kTopCap = 384;      // candidates > theta held in shared memory per row
+constexpr int kTopHits = 2 * kMaxK;  // tiles reaching theta listed per row (aliases the selection slots)
+constexpr int kThKeys = 32;       // tile maxima per lane kept in registers (more are re-read)
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
     topk_rows_kernel(const float* __restrict__ part_m, const float* __restrict__ top_v,
-                     const int* __restrict__ top_i, int stride, int ntiles, int rows, int K,
+                     const int* __restrict__ top_i, int stride, int ntiles, int rows, int K, int sub_rows,
                      float* __restrict__ theta, int* __restrict__ cnt_gt, int* __restrict__ cnt_eq,
-                     uint8_t* __restrict__ row_flag, int* __restrict__ any_flag, int32_t* __restrict__ idx_out,
+                     uint8_t* __restrict__ row_flag, int* __restrict__ sub_flag, int32_t* __restrict__ idx_out,
                      float* __restrict__ logit_out) {
     __shared__ uint32_t s_key[kRowsPerBlock][kTopCap];
     __shared__ int s_id[kRowsPerBlock][kTopCap];
     __shared__ int s_tie[kRowsPerBlock][kMaxK];
-    __shared__ uint32_t s_skey[kRowsPerBlock][kMaxK];
-    __shared__ int s_sid[kRowsPerBlock][kMaxK];
+    // per warp: the selection's keys [0, kMaxK) and ids [kMaxK, 2 kMaxK); the tile list before it
+    __shared__ uint32_t s_sel[kRowsPerBlock][2 * kMaxK];
+    static_assert(kTopHits <= 2 * kMaxK, "the tile list fits the selection slots");
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t* const s_skey = s_sel[w];
+    int* const s_sid = reinterpret_cast<int*>(s_sel[w] + kMaxK);
+    int* const s_hit = reinterpret_cast<int*>(s_sel[w]);
     const int r = blockIdx.x * kRowsPerBlock + w;
     if (r >= rows) return;  // whole warps only; no block-wide barrier follows
     const unsigned lt = (1u << lane) - 1u;
-    const float th = row_theta(part_m, stride, ntiles, r, K, lane);
 
-    // gather: lanes take tiles in turn; ballots keep the lists in tile order
-    int n_gt = 0, n_eq = 0;
-    bool flag = false;
-    const int nround = (ntiles + 31) & ~31;
-    for (int n0 = 0; n0 < nround; n0 += 32) {
+    // 1. theta
+    uint32_t key[kThKeys];
+#pragma unroll
+    for (int j = 0; j < kThKeys; ++j) {
+        const int n = lane + 32 * j;
+        key[j] = n < ntiles ? fkey(part_m[static_cast<size_t>(n) * stride + r]) : 0u;
+    }
+    uint32_t t = 0;  // largest key with at least K tile maxima at or above it
+    if (ntiles >= K) {
+        for (int b = 31; b >= 0; --b) {
+            const uint32_t cand = t | (1u << b);
+            int c = 0;
+#pragma unroll
+            for (int j = 0; j < kThKeys; ++j) c += key[j] >= cand;
+            for (int n = lane + 32 * kThKeys; n < ntiles; n += 32)
+                c += fkey(part_m[static_cast<size_t>(n) * stride + r]) >= cand;
+            if (warp_sum(c) >= K) t = cand;
+        }
+    }
+    const float th = ntiles >= K ? unkey(t) : -INFINITY;
+    const uint32_t tkey = fkey(th);
+
+    // 2. the tiles reaching theta, then their kept logits
+    int n_hit = 0;
+#pragma unroll
+    for (int j = 0; j < kThKeys; ++j) {
+        const int n = lane + 32 * j;
+        const bool hit = n < ntiles && key[j] >= tkey;
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (hit && n_hit + __popc(m & lt) < kTopHits) s_hit[n_hit + __popc(m & lt)] = n;
+        n_hit += __popc(m);
+    }
+    for (int n0 = 32 * kThKeys; n0 < ntiles; n0 += 32) {
         const int n = n0 + lane;
+        const bool hit = n < ntiles && fkey(part_m[static_cast<size_t>(n) * stride + r]) >= tkey;
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (hit && n_hit + __popc(m & lt) < kTopHits) s_hit[n_hit + __popc(m & lt)] = n;
+        n_hit += __popc(m);
+    }
+    __syncwarp();
+    bool flag = n_hit > kTopHits;
+    int n_gt = 0, n_eq = 0;
+    for (int i0 = 0; i0 < n_hit && !flag; i0 += 32) {
+        const int i = i0 + lane;
         float v[kTopPerTile];
         int id[kTopPerTile];
-        const size_t o = static_cast<size_t>(n) * stride + r;
-        const bool hit = n < ntiles && part_m[o] >= th;
 #pragma unroll
         for (int e = 0; e < kTopPerTile; ++e) {
             v[e] = -INFINITY;
             id[e] = INT_MAX;
         }
-        if (hit) {
+        const bool have = i < n_hit;
+        if (have) {
+            const size_t o = static_cast<size_t>(s_hit[i]) * stride + r;
 #pragma unroll
             for (int q4 = 0; q4 < kTopPerTile / 4; ++q4) {
                 const float4 a = reinterpret_cast<const float4*>(top_v)[o * (kTopPerTile / 4) + q4];
@@ -448,15 +471,14 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
                 v[4 * q4] = a.x, v[4 * q4 + 1] = a.y, v[4 * q4 + 2] = a.z, v[4 * q4 + 3] = a.w;
                 id[4 * q4] = b.x, id[4 * q4 + 1] = b.y, id[4 * q4 + 2] = b.z, id[4 * q4 + 3] = b.w;
             }
-            flag = flag || v[kTopPerTile - 1] >= th;
         }
-        if (__any_sync(0xffffffffu, flag)) {
+        if (__any_sync(0xffffffffu, have && v[kTopPerTile - 1] >= th)) {
             flag = true;
             break;
         }
 #pragma unroll
         for (int e = 0; e < kTopPerTile - 1; ++e) {
-            const bool gt = hit && v[e] > th, eq = hit && v[e] == th;
+            const bool gt = have && v[e] > th, eq = have && v[e] == th;
             const unsigned mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
             if (gt) {
                 const int slot = n_gt + __popc(mg & lt);
@@ -479,26 +501,26 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
             cnt_gt[r] = 0;
             cnt_eq[r] = 0;
             row_flag[r] = 1;
-            atomicExch(any_flag, 1);
+            atomicExch(sub_flag + r / sub_rows, 1);
         }
         return;
     }
     if (lane == 0) row_flag[r] = 0;
     __syncwarp();
 
-    // selection into s_skey / s_sid [0, K)
+    // 3. selection into s_skey / s_sid [0, K), then the sort
     if (n_gt >= K) {
-        uint32_t t = 0;  // key of the K-th largest candidate
+        uint32_t tk = 0;  // key of the K-th largest candidate
         for (int b = 31; b >= 0; --b) {
-            const uint32_t cand = t | (1u << b);
+            const uint32_t cand = tk | (1u << b);
             int c = 0;
             for (int i = lane; i < n_gt; i += 32) c += s_key[w][i] >= cand;
-            if (warp_sum(c) >= K) t = cand;
+            if (warp_sum(c) >= K) tk = cand;
         }
         int above = 0, at = 0;
         for (int i = lane; i < n_gt; i += 32) {
-            above += s_key[w][i] > t;
-            at += s_key[w][i] == t;
+            above += s_key[w][i] > tk;
+            at += s_key[w][i] == tk;
         }
         above = warp_sum(above);
         at = warp_sum(at);
@@ -510,7 +532,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
                 const uint32_t c2 = cut | (1u << b);
                 int c = 0;
                 for (int i = lane; i < n_gt; i += 32)
-                    c += s_key[w][i] == t && static_cast<uint32_t>(s_id[w][i]) < c2;
+                    c += s_key[w][i] == tk && static_cast<uint32_t>(s_id[w][i]) < c2;
                 if (warp_sum(c) < need) cut = c2;
             }
         }
@@ -524,32 +546,31 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
             if (i < n_gt) {
                 kk = s_key[w][i];
                 ii = s_id[w][i];
-                keep = kk > t || (kk == t && static_cast<uint32_t>(ii) <= cut);
+                keep = kk > tk || (kk == tk && static_cast<uint32_t>(ii) <= cut);
             }
             const unsigned mk = __ballot_sync(0xffffffffu, keep);
             if (keep) {
                 const int slot = m + __popc(mk & lt);
-                s_skey[w][slot] = kk;
-                s_sid[w][slot] = ii;
+                s_skey[slot] = kk;
+                s_sid[slot] = ii;
             }
             m += __popc(mk);
         }
     } else {
-        const uint32_t tk = fkey(th);
         for (int i = lane; i < n_gt; i += 32) {
-            s_skey[w][i] = s_key[w][i];
-            s_sid[w][i] = s_id[w][i];
+            s_skey[i] = s_key[w][i];
+            s_sid[i] = s_id[w][i];
         }
         for (int i = lane; i < K - n_gt; i += 32) {  // at least K - n_gt ties exist (K tiles reach theta)
-            s_skey[w][n_gt + i] = tk;
-            s_sid[w][n_gt + i] = s_tie[w][i];
+            s_skey[n_gt + i] = tkey;
+            s_sid[n_gt + i] = s_tie[w][i];
         }
     }
     int P = 1;
     while (P < K) P <<= 1;
     for (int i = K + lane; i < P; i += 32) {
-        s_skey[w][i] = 0u;  // below every real key: sorts last
-        s_sid[w][i] = INT_MAX;
+        s_skey[i] = 0u;  // below every real key: sorts last
+        s_sid[i] = INT_MAX;
     }
     __syncwarp();
     // bitonic sort of the P slots: key descending, id ascending
@@ -559,14 +580,14 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
                 const int j = i ^ str;
                 if (j > i) {
                     const bool desc = (i & size) == 0;
-                    const uint32_t ki = s_skey[w][i], kj = s_skey[w][j];
-                    const int ii = s_sid[w][i], ij = s_sid[w][j];
+                    const uint32_t ki = s_skey[i], kj = s_skey[j];
+                    const int ii = s_sid[i], ij = s_sid[j];
                     const bool i_first = ki > kj || (ki == kj && ii < ij);
                     if (i_first != desc) {
-                        s_skey[w][i] = kj;
-                        s_skey[w][j] = ki;
-                        s_sid[w][i] = ij;
-                        s_sid[w][j] = ii;
+                        s_skey[i] = kj;
+                        s_skey[j] = ki;
+                        s_sid[i] = ij;
+                        s_sid[j] = ii;
                     }
                 }
             }
@@ -574,8 +595,8 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
         }
     }
     for (int k = lane; k < K; k += 32) {
-        idx_out[static_cast<size_t>(r) * K + k] = s_sid[w][k];
-        logit_out[static_cast<size_t>(r) * K + k] = unkey(s_skey[w][k]);
+        idx_out[static_cast<size_t>(r) * K + k] = s_sid[k];
+        logit_out[static_cast<size_t>(r) * K + k] = unkey(s_skey[k]);
     }
 }
 
@@ -699,11 +720,23 @@ void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const i
 }
 
 void launch_topk_rows(const float* part_m, const float* top_v, const int* top_i, int part_stride, int ntiles,
-                      int rows, int K, float* theta, int* cnt_gt, int* cnt_eq, uint8_t* row_flag, int* any_flag,
-                      int32_t* idx_out, float* logit_out, cudaStream_t s) {
+                      int rows, int K, int sub_rows, float* theta, int* cnt_gt, int* cnt_eq, uint8_t* row_flag,
+                      int* sub_flag, int32_t* idx_out, float* logit_out, cudaStream_t s) {
     topk_rows_kernel<<<(rows + kRowsPerBlock - 1) / kRowsPerBlock, 32 * kRowsPerBlock, 0, s>>>(
-        part_m, top_v, top_i, part_stride, ntiles, rows, K, theta, cnt_gt, cnt_eq, row_flag, any_flag, idx_out,
-        logit_out);
+        part_m, top_v, top_i, part_stride, ntiles, rows, K, sub_rows, theta, cnt_gt, cnt_eq, row_flag, sub_flag,
+        idx_out, logit_out);
+}
+
+// *out |= any of flags[0, n): the teacher top-K call's record that some row took
+// the second tensor-core pass.
+__global__ void or_flags_kernel(const int* __restrict__ flags, int n, int* __restrict__ out) {
+    int f = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) f |= flags[i];
+    if (__syncthreads_or(f) && threadIdx.x == 0) *out = 1;
+}
+
+void launch_or_flags(const int* flags, int n, int* out, cudaStream_t s) {
+    or_flags_kernel<<<1, 256, 0, s>>>(flags, n, out);
 }
 
 // dh *= g (bf16, rounded once more to nearest even) and dW *= g (fp32), with the

@@ -115,7 +115,7 @@ const char* const kKindNames[KK_NUM] = {
     "bwd_gemm_dz", "bwd_gemm_dh", "dh_reduce", "bwd_gemm_dw", "selftest_gemm",
     "fb_gemm_lse_keep", "fb_dz_from_logits",
     "tk_gemm_tile_top8", "tk_rows", "tk_gemm_candidates", "tk_select_flagged", "selftest_wait", "scale_grads",
-    "transpose_h",
+    "transpose_h", "tk_flags",
 };
 
 // ---------------------------------------------------------------- device facts
@@ -335,12 +335,16 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
 }
 
 // ---------------------------------------------------------------- teacher top-K plan
-constexpr int kDefaultTopkChunk = 1024;
+// Rows per chunk of the first tensor-core pass and the per-row selection (enough
+// warps for the selection to hide its memory latency), and per sub-chunk of the
+// second pass, whose candidate lists are sized for the worst case of every row.
+constexpr int kDefaultTopkChunk = 4096;
+constexpr int kTopkSubChunk = 1024;
 
 struct TopkPlan {
     int64_t N, V, n_chunks;
-    int d, K, Cc, nt_v, cap;
-    size_t o_part, o_topv, o_topi, o_theta, o_gt, o_eq, o_flag, o_cv, o_ci, o_tie, total;
+    int d, K, Cc, Cs, n_sub, nt_v, cap;
+    size_t o_part, o_topv, o_topi, o_theta, o_gt, o_eq, o_flag, o_sflag, o_cv, o_ci, o_tie, total;
 };
 
 bool make_topk_plan(int64_t N, int d, int64_t V, int K, int chunk, TopkPlan& P) {
@@ -352,6 +356,8 @@ bool make_topk_plan(int64_t N, int d, int64_t V, int K, int chunk, TopkPlan& P) 
     const int64_t want = chunk > 0 ? chunk : kDefaultTopkChunk;
     P.Cc = static_cast<int>(std::min<int64_t>(want, cdiv(N, kBM) * kBM));
     P.n_chunks = cdiv(N, P.Cc);
+    P.Cs = std::min(P.Cc, kTopkSubChunk);
+    P.n_sub = static_cast<int>(cdiv(P.Cc, P.Cs));
     P.nt_v = static_cast<int>(cdiv(V, kVocabTile));
     // logits above the threshold lie in fewer than K vocabulary tiles (or the
     // threshold is -inf and there are fewer than K tiles in all)
@@ -371,12 +377,14 @@ bool make_topk_plan(int64_t N, int d, int64_t V, int K, int chunk, TopkPlan& P) 
     off += align256(size_t(P.Cc) * 4);
     P.o_eq = off;
     off += align256(size_t(P.Cc) * 4);
-    P.o_cv = off;
-    off += align256(size_t(P.Cc) * P.cap * 4);
+    P.o_sflag = off;  // one word per sub-chunk: some row of it needs the second pass
+    off += align256(size_t(P.n_sub) * 4);
+    P.o_cv = off;  // candidate and tie lists: one sub-chunk's rows
+    off += align256(size_t(P.Cs) * P.cap * 4);
     P.o_ci = off;
-    off += align256(size_t(P.Cc) * P.cap * 4);
+    off += align256(size_t(P.Cs) * P.cap * 4);
     P.o_tie = off;
-    off += align256(size_t(P.Cc) * K * 4);
+    off += align256(size_t(P.Cs) * K * 4);
     P.total = off;
     return true;
 }
@@ -953,7 +961,7 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* w = static_cast<char*>(ws);
     int* status = reinterpret_cast<int*>(w);
-    int* any_flag = status + 1;
+    int* any_flag = status + 1;  // some row of the call needed the second pass (diagnostic)
     float* part = reinterpret_cast<float*>(w + P.o_part);
     float* top_v = reinterpret_cast<float*>(w + P.o_topv);
     int* top_i = reinterpret_cast<int*>(w + P.o_topi);
@@ -961,6 +969,7 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
     float* theta = reinterpret_cast<float*>(w + P.o_theta);
     int* cnt_gt = reinterpret_cast<int*>(w + P.o_gt);
     int* cnt_eq = reinterpret_cast<int*>(w + P.o_eq);
+    int* sub_flag = reinterpret_cast<int*>(w + P.o_sflag);
     float* cand_v = reinterpret_cast<float*>(w + P.o_cv);
     int* cand_i = reinterpret_cast<int*>(w + P.o_ci);
     int* tie_i = reinterpret_cast<int*>(w + P.o_tie);
@@ -973,9 +982,9 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
         const int64_t row0 = c * P.Cc;
         const int rows = static_cast<int>(std::min<int64_t>(P.Cc, N - row0));
         const double flop = 2.0 * rows * double(d) * double(V);
+        const char* hc = static_cast<const char*>(h) + size_t(row0) * d * 2;
         CUtensorMap tmH;
-        FKL_TMAP(tmH, BF16, static_cast<const char*>(h) + size_t(row0) * d * 2, uint64_t(d), uint64_t(rows),
-                 uint64_t(d) * 2, 64, 128);
+        FKL_TMAP(tmH, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 128);
         GemmParams p{};
         p.m_tiles = static_cast<int>(cdiv(rows, kPairRows));
         p.n_tiles = P.nt_v;
@@ -990,26 +999,46 @@ fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int6
         p.top_i = top_i;
         p.part_stride = P.Cc;
         p.K = K;
-        FKL_CUDA_TRY(cudaMemsetAsync(any_flag, 0, sizeof(int), s));
+        FKL_CUDA_TRY(cudaMemsetAsync(sub_flag, 0, size_t(P.n_sub) * 4, s));
         if (fkl_status st = run_gemm(KK_TK_GEMM_TMAX, 256, 0, 0, EPI_TMAX, tmH, tmW, tmW, p, flop, s)) return st;
         // theta, candidates and selection per row; rows it cannot complete are flagged
-        FKL_SMALL(KK_TK_ROWS, launch_topk_rows(part, top_v, top_i, P.Cc, P.nt_v, rows, K, theta, cnt_gt, cnt_eq,
-                                               row_flag, any_flag, idx + size_t(row0) * K, logit + size_t(row0) * K,
-                                               s));
-        // the second tensor-core pass, for the flagged rows; it returns at once if none is
-        p.any_flag = any_flag;
-        p.row_flag = row_flag;
-        p.theta = theta;
-        p.cnt_gt = cnt_gt;
-        p.cnt_eq = cnt_eq;
-        p.cand_v = cand_v;
-        p.cand_i = cand_i;
-        p.cand_cap = P.cap;
-        p.tie_i = tie_i;
-        // (its FLOP are not counted: the launch usually returns at once)
-        if (fkl_status st = run_gemm(KK_TK_GEMM_CAND, 256, 0, 0, EPI_CAND, tmH, tmW, tmW, p, 0.0, s)) return st;
-        FKL_SMALL(KK_TK_SELECT, launch_topk_select(cand_v, cand_i, P.cap, cnt_gt, cnt_eq, tie_i, theta, row_flag, rows,
-                                                   K, idx + size_t(row0) * K, logit + size_t(row0) * K, s));
+        FKL_SMALL(KK_TK_ROWS, launch_topk_rows(part, top_v, top_i, P.Cc, P.nt_v, rows, K, P.Cs, theta, cnt_gt,
+                                               cnt_eq, row_flag, sub_flag, idx + size_t(row0) * K,
+                                               logit + size_t(row0) * K, s));
+        // the second tensor-core pass and the selection of its rows, per sub-chunk
+        // with a flagged row (a launch returns at once when its sub-chunk has none)
+        for (int r0 = 0; r0 < rows; r0 += P.Cs) {
+            const int srows = std::min(P.Cs, rows - r0);
+            const int sc = r0 / P.Cs;
+            CUtensorMap tmHs;
+            FKL_TMAP(tmHs, BF16, hc + size_t(r0) * d * 2, uint64_t(d), uint64_t(srows), uint64_t(d) * 2, 64, 128);
+            GemmParams q{};
+            q.m_tiles = static_cast<int>(cdiv(srows, kPairRows));
+            q.n_tiles = P.nt_v;
+            q.splits = 1;
+            q.kb_total = static_cast<int>(cdiv(d, kBK));
+            q.m_fastest = 1;
+            q.M = srows;
+            q.Ncols = static_cast<int>(V);
+            q.status = status;
+            q.K = K;
+            q.any_flag = sub_flag + sc;
+            q.row_flag = row_flag + r0;
+            q.theta = theta + r0;
+            q.cnt_gt = cnt_gt + r0;
+            q.cnt_eq = cnt_eq + r0;
+            q.cand_v = cand_v;
+            q.cand_i = cand_i;
+            q.cand_cap = P.cap;
+            q.tie_i = tie_i;
+            // (its FLOP are not counted: the launch usually returns at once)
+            if (fkl_status st = run_gemm(KK_TK_GEMM_CAND, 256, 0, 0, EPI_CAND, tmHs, tmW, tmW, q, 0.0, s)) return st;
+            FKL_SMALL(KK_TK_SELECT,
+                      launch_topk_select(cand_v, cand_i, P.cap, cnt_gt + r0, cnt_eq + r0, tie_i, theta + r0,
+                                         row_flag + r0, srows, K, idx + size_t(row0 + r0) * K,
+                                         logit + size_t(row0 + r0) * K, s));
+        }
+        FKL_SMALL(KK_TK_FLAGS, launch_or_flags(sub_flag, P.n_sub, any_flag, s));
     }
     return FKL_OK;
 }

@@ -40,6 +40,7 @@ enum KernelKind {
     KK_SELFTEST_WAIT,  // bounded-wait self-test
     KK_SCALE_GRADS,    // dh, dW times an upstream gradient
     KK_TRANSPOSE_H,    // h of a chunk transposed: the dW GEMM's K-major operand
+    KK_TK_FLAGS,       // teacher top-K: the call's second-pass flag from the sub-chunks' flags
     KK_NUM
 };
 
@@ -131,11 +132,12 @@ void launch_loss_reduce(const float* rowloss, int64_t N, const int* n_valid, flo
 void launch_dh_reduce(const float* part, int splits, size_t split_elems, int rows, int d, void* dh,
                       cudaStream_t s);
 void launch_topk_rows(const float* part_m, const float* top_v, const int* top_i, int part_stride, int ntiles,
-                      int rows, int K, float* theta, int* cnt_gt, int* cnt_eq, uint8_t* row_flag, int* any_flag,
-                      int32_t* idx_out, float* logit_out, cudaStream_t s);
+                      int rows, int K, int sub_rows, float* theta, int* cnt_gt, int* cnt_eq, uint8_t* row_flag,
+                      int* sub_flag, int32_t* idx_out, float* logit_out, cudaStream_t s);
 void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const int* cnt_gt, const int* cnt_eq,
                         const int* tie_i, const float* theta, const uint8_t* row_flag, int rows, int K,
                         int32_t* idx_out, float* logit_out, cudaStream_t s);
+void launch_or_flags(const int* flags, int n, int* out, cudaStream_t s);
 void launch_scale_grads(void* dh, size_t n_dh, float* dW, size_t n_dw, const float* g, int grid, cudaStream_t s);
 void launch_dz_from_logits(void* yz, int64_t pstride, int64_t V, const float* part_m, int part_stride,
                            const float* lse, const uint8_t* valid, const int* n_valid, const float* grad,
