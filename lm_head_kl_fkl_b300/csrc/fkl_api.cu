@@ -202,12 +202,12 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 // panels `panel_bytes` apart, each a [rows][64] bf16 (or fp16) array; 128-byte
 // swizzle.  Every box {64, box_rows, 1} is one contiguous run of box_rows x 128 bytes.
 bool make_panel_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t rows, uint64_t panels,
-                     uint64_t panel_bytes, uint32_t box_rows) {
+                     uint64_t panel_bytes, uint32_t box_rows, uint32_t box_panels = 1) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {64, rows, panels};
     cuuint64_t strides[2] = {128, panel_bytes};
-    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t box[3] = {64, box_rows, box_panels};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -431,10 +431,10 @@ fkl_status run_gemm(int kind, int bn, int a_mn, int b_mn, int epi, const CUtenso
     } while (0)
 
 // Panel map of the chunk's dz (or kept-logit) buffer with boxes of box_rows rows.
-#define FKL_PANEL_TMAP(m, dt, base, box_rows)                                                       \
+#define FKL_PANEL_TMAP(m, dt, base, box_rows, ...)                                                  \
     do {                                                                                            \
         if (!make_panel_tmap(&(m), dt, base, uint64_t(rows), uint64_t(P.npan), uint64_t(P.Cc) * 128, \
-                             box_rows))                                                             \
+                             box_rows, ##__VA_ARGS__))                                              \
             return fail(FKL_ERR_CUDA, "cuTensorMapEncodeTiled failed for " #m);                     \
     } while (0)
 
@@ -624,7 +624,7 @@ fkl_status backward_enqueue(const Plan& P, const void* h, const void* W, const i
                  uint32_t(std::min(P.bn_dw, 256) / 2));
         FKL_PANEL_TMAP(tmDz_st, BF16, dz, 32);
         FKL_PANEL_TMAP(tmDz_k, BF16, dz, 128);
-        FKL_PANEL_TMAP(tmDz_mn, BF16, dz, 64);
+        FKL_PANEL_TMAP(tmDz_mn, BF16, dz, 64, 2);  // dW's A: the two panels of a CTA's 128 rows in one box
         FKL_TMAP(tmPart, F32, part, uint64_t(d), uint64_t(P.splits) * P.Cc, uint64_t(d) * 4, 32, 32);
         FKL_SMALL(KK_TRANSPOSE_H, launch_transpose_h(hc, rows, d, hT, P.Cc, s));
 
@@ -902,7 +902,7 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
                  uint32_t(std::min(P.bn_dw, 256) / 2));
         FKL_PANEL_TMAP(tmY_st, F16, yz, 32);
         FKL_PANEL_TMAP(tmDz_k, BF16, yz, 128);
-        FKL_PANEL_TMAP(tmDz_mn, BF16, yz, 64);
+        FKL_PANEL_TMAP(tmDz_mn, BF16, yz, 64, 2);
         FKL_TMAP(tmPart, F32, part, uint64_t(d), uint64_t(P.splits) * P.Cc, uint64_t(d) * 4, 32, 32);
         FKL_SMALL(KK_TRANSPOSE_H, launch_transpose_h(hc, rows, d, hT, P.Cc, s));
 

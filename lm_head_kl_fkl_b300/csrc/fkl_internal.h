@@ -63,7 +63,7 @@ constexpr bool epi_staged(int epi) {
 struct GemmParams {
     int m_tiles, n_tiles, splits, kb_total, m_fastest;
     int M;             // valid rows of the output (rows beyond are not written)
-    int a_panel;       // 1: A is the dz panel buffer, a 3-D map {64 columns, rows, panel}
+    int a_panel;       // 1: A is the dz panel buffer, a 3-D map {64 columns, rows, panel} (MN-major: boxes of 2 panels)
     int Ncols;         // valid columns (V for the logit GEMMs, d for dh / dW)
     int* status;       // device status word
     // EPI_LSE / EPI_DZ

@@ -256,9 +256,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (A_MN == 0) {
                         if (p.a_panel) tma_load_3d_pair(sa, &tmA, fb, 0, arow, kb);
                         else tma_load_2d_pair(sa, &tmA, fb, kb * kBK, arow);
-                    } else if (p.a_panel) {  // the CTA's 128 A rows are two 64-column panels
+                    } else if (p.a_panel) {
+                        // the two 64-column panels of the CTA's 128 A rows in one box {64, 64, 2}:
+                        // each TMA instruction costs the producer about 100 cycles, whatever its size
                         tma_load_3d_pair(sa, &tmA, fb, 0, kb * kBK, arow >> 6);
-                        tma_load_3d_pair(sa + 8192u, &tmA, fb, 0, kb * kBK, (arow >> 6) + 1);
                     } else {
                         tma_load_2d_pair(sa, &tmA, fb, arow, kb * kBK);
                         tma_load_2d_pair(sa + 8192u, &tmA, fb, arow + 64, kb * kBK);
