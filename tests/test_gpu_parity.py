@@ -39,6 +39,7 @@ SHAPES = [
     (640, 256, 4096, 100, 2.0, "zipf1.1", 256),      # many teacher hits in the first vocab tiles
     (130, 384, 2304, 32, 0.5, "half-student", 0),    # teacher overlaps the student's top-K
     (96, 200, 777, 5, 1.0, "uniform", 0),            # everything ragged, N below one tile
+    (1000, 96, 2500, 20, 1.0, "uniform", 384),       # chunk not a multiple of the 256-row pair tile
 ]
 
 

@@ -58,6 +58,9 @@ CASES = [
     (300, 256, 5000, 100),
     (130, 64, 777, 1),
     (64, 64, 256, 256),
+    # the largest K over many tiles: rows may hold more candidates than the per-row
+    # shared-memory list and take the second pass
+    (64, 64, 70000, 256),
 ]
 
 
