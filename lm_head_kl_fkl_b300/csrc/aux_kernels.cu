@@ -258,65 +258,129 @@ __global__ void dh_reduce_kernel(const float4* __restrict__ part, int splits, si
     }
 }
 
-// dz of one chunk row from the logits its forward kept: y = z log2e/T - m_tile
-// (fp16, m_tile = part_m[tile][row], base 2), dz = coef (2^(y + m_tile - lse log2e)
-// - s) in bf16, written over y in place.  One block per row: the y at the teacher
-// ids are read first, then the whole row is rewritten, then the teacher entries
-// (each run of equal ids once, its p summed) are written with s subtracted.
-__global__ void dz_from_logits_kernel(uint16_t* __restrict__ yz, int64_t pstride, int64_t V,
-                                      const float* __restrict__ part_m, int stride,
-                                      const float* __restrict__ lse, const uint8_t* __restrict__ valid,
-                                      const int* __restrict__ n_valid, const float* __restrict__ grad, float T,
-                                      const int* __restrict__ sidx, const float* __restrict__ sp, int K) {
-    __shared__ float s_y[kMaxK];
+// dz of one chunk from the logits its forward kept: y = z log2e/T - m_tile (fp16,
+// m_tile = part_m[tile][row], base 2), dz = coef (2^(y + m_tile - lse log2e) - s) in
+// bf16, written over y in place, in three launches:
+//  1. teacher_y_kernel (a warp per row): y + m_tile at the row's teacher ids, kept in
+//     yk [rows][K] before they are overwritten;
+//  2. dz_panels_kernel (a block per 64 rows x kDzPanels panels): coef 2^(y + m_tile -
+//     lse log2e) over the panels, each a contiguous 64 x 128-byte run;
+//  3. teacher_dz_kernel (a warp per row): the teacher entries (each run of equal ids
+//     once, its p summed) rewritten with s subtracted, from yk.
+// Element (r, v) of the panel layout is yz[(v / 64) pstride + 64 r + v % 64].
+struct DzRow {
+    float lse2, coef;
+};
+__device__ __forceinline__ DzRow dz_row(const float* lse, const uint8_t* valid, const int* n_valid,
+                                        const float* grad, float T, int r) {
     constexpr float kLog2eF = 1.4426950408889634f;
-    const int r = blockIdx.x;
-    // element (r, v) of the panel layout: panel v / 64, row r, column v % 64
-    uint16_t* row = yz + static_cast<size_t>(r) * 64;
-    auto at = [&](int64_t v) -> uint16_t* { return row + (v >> 6) * pstride + (v & 63); };
+    const int nv = *n_valid;
+    DzRow d;
+    d.lse2 = lse[r] * kLog2eF;
+    d.coef = (valid[r] && nv > 0) ? T * (grad ? *grad : 1.f) / static_cast<float>(nv) : 0.f;
+    return d;
+}
+
+__global__ void teacher_y_kernel(const uint16_t* __restrict__ yz, int64_t pstride, int64_t V,
+                                 const float* __restrict__ part_m, int stride, const int* __restrict__ sidx, int K,
+                                 int rows, float* __restrict__ yk) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    for (int k = lane; k < K; k += 32) {
+        const int v = sidx[static_cast<size_t>(r) * K + k];
+        float y = 0.f;
+        if (v < V)
+            y = __half2float(__ushort_as_half(yz[(v >> 6) * pstride + static_cast<int64_t>(r) * 64 + (v & 63)])) +
+                part_m[static_cast<size_t>(v >> 8) * stride + r];
+        yk[static_cast<size_t>(r) * K + k] = y;
+    }
+}
+
+constexpr int kDzRows = 64;    // rows per block of dz_panels_kernel
+constexpr int kDzPanels = 16;  // panels per block
+
+__global__ void __launch_bounds__(256)
+    dz_panels_kernel(uint16_t* __restrict__ yz, int64_t pstride, int64_t npan, int64_t V,
+                     const float* __restrict__ part_m, int stride, const float* __restrict__ lse,
+                     const uint8_t* __restrict__ valid, const int* __restrict__ n_valid, const float* __restrict__ grad,
+                     float T, int rows) {
+    __shared__ float s_coef[kDzRows], s_lse2[kDzRows], s_shift[kDzRows];
+    const int t = threadIdx.x;
+    const int r0 = blockIdx.x * kDzRows;
+    const int64_t p0 = static_cast<int64_t>(blockIdx.y) * kDzPanels;
+    if (t < kDzRows) {
+        DzRow d{0.f, 0.f};
+        if (r0 + t < rows) d = dz_row(lse, valid, n_valid, grad, T, r0 + t);
+        s_coef[t] = d.coef;
+        s_lse2[t] = d.lse2;
+    }
+    const int64_t p1 = p0 + kDzPanels < npan ? p0 + kDzPanels : npan;
+    for (int64_t p = p0; p < p1; ++p) {
+        if (p == p0 || (p & 3) == 0) {  // a 256-column tile spans four panels
+            __syncthreads();
+            if (t < kDzRows && r0 + t < rows)
+                s_shift[t] = part_m[static_cast<size_t>(p >> 2) * stride + r0 + t] - s_lse2[t];
+            __syncthreads();
+        }
+        uint16_t* base = yz + p * pstride + static_cast<int64_t>(r0) * 64;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int c = t + 256 * i;  // chunk of 8 columns: row c / 8, columns (c % 8) * 8 ...
+            const int row = c >> 3, col = (c & 7) * 8;
+            if (r0 + row >= rows) continue;
+            uint4* p8 = reinterpret_cast<uint4*>(base + row * 64 + col);
+            const uint4 in = *p8;
+            const float shift = s_shift[row], coef = s_coef[row];
+            const int64_t v = p * 64 + col;
+            const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+                const float a = (v + 2 * j < V) ? coef * exp2f(y.x + shift) : 0.f;
+                const float b = (v + 2 * j + 1 < V) ? coef * exp2f(y.y + shift) : 0.f;
+                const __nv_bfloat162 ab = __floats2bfloat162_rn(a, b);
+                o[j] = *reinterpret_cast<const uint32_t*>(&ab);
+            }
+            *p8 = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+__global__ void teacher_dz_kernel(uint16_t* __restrict__ yz, int64_t pstride, int64_t V,
+                                  const float* __restrict__ lse, const uint8_t* __restrict__ valid,
+                                  const int* __restrict__ n_valid, const float* __restrict__ grad, float T,
+                                  const int* __restrict__ sidx, const float* __restrict__ sp, int K, int rows,
+                                  const float* __restrict__ yk) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const DzRow d = dz_row(lse, valid, n_valid, grad, T, r);
     const int* ids = sidx + static_cast<size_t>(r) * K;
     const float* ps = sp + static_cast<size_t>(r) * K;
-    const float lse2 = lse[r] * kLog2eF;
-    const int nv = *n_valid;
-    const float coef = (valid[r] && nv > 0) ? T * (grad ? *grad : 1.f) / static_cast<float>(nv) : 0.f;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-        const int v = ids[k];
-        s_y[k] = (v < V) ? __half2float(__ushort_as_half(*at(v))) + part_m[static_cast<size_t>(v >> 8) * stride + r]
-                         : 0.f;
-    }
-    __syncthreads();
-    for (int64_t v = static_cast<int64_t>(threadIdx.x) * 8; v < V; v += static_cast<int64_t>(blockDim.x) * 8) {
-        uint4* p8 = reinterpret_cast<uint4*>(at(v));  // 8 columns inside one panel
-        const uint4 in = *p8;
-        const float shift = part_m[static_cast<size_t>(v >> 8) * stride + r] - lse2;
-        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-            const float a = (v + 2 * j < V) ? coef * exp2f(y.x + shift) : 0.f;
-            const float b = (v + 2 * j + 1 < V) ? coef * exp2f(y.y + shift) : 0.f;
-            const __nv_bfloat162 ab = __floats2bfloat162_rn(a, b);
-            o[j] = *reinterpret_cast<const uint32_t*>(&ab);
-        }
-        *p8 = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    __syncthreads();
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    for (int k = lane; k < K; k += 32) {
         const int v = ids[k];
         if (v >= V || (k > 0 && ids[k - 1] == v)) continue;
         float s = ps[k];
         for (int j = k + 1; j < K && ids[j] == v; ++j) s += ps[j];
-        const __nv_bfloat16 d = __float2bfloat16_rn(coef * (exp2f(s_y[k] - lse2) - s));
-        *at(v) = __bfloat16_as_ushort(d);
+        const __nv_bfloat16 dz = __float2bfloat16_rn(d.coef * (exp2f(yk[static_cast<size_t>(r) * K + k] - d.lse2) - s));
+        yz[(v >> 6) * pstride + static_cast<int64_t>(r) * 64 + (v & 63)] = __bfloat16_as_ushort(dz);
     }
 }
 
 void launch_dz_from_logits(void* yz, int64_t pstride, int64_t V, const float* part_m, int part_stride,
                            const float* lse, const uint8_t* valid, const int* n_valid, const float* grad,
-                           float T, const int* sidx, const float* sp, int K, int rows, cudaStream_t s) {
-    dz_from_logits_kernel<<<rows, 256, 0, s>>>(static_cast<uint16_t*>(yz), pstride, V, part_m, part_stride, lse,
-                                               valid, n_valid, grad, T, sidx, sp, K);
+                           float T, const int* sidx, const float* sp, int K, int rows, float* yk, cudaStream_t s) {
+    uint16_t* y = static_cast<uint16_t*>(yz);
+    const int64_t npan = (V + 63) / 64;
+    teacher_y_kernel<<<(rows + 7) / 8, 256, 0, s>>>(y, pstride, V, part_m, part_stride, sidx, K, rows, yk);
+    const dim3 grid(static_cast<unsigned>((rows + kDzRows - 1) / kDzRows),
+                    static_cast<unsigned>((npan + kDzPanels - 1) / kDzPanels));
+    dz_panels_kernel<<<grid, 256, 0, s>>>(y, pstride, npan, V, part_m, part_stride, lse, valid, n_valid, grad, T,
+                                          rows);
+    teacher_dz_kernel<<<(rows + 7) / 8, 256, 0, s>>>(y, pstride, V, lse, valid, n_valid, grad, T, sidx, sp, K, rows,
+                                                     yk);
 }
 
 // ---------------------------------------------------------------- h transposed

@@ -224,7 +224,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 struct Plan {
     int64_t N, V, npan, n_chunks;  // npan: 64-column panels of the dz buffer
     int d, K, Cc, nt_v, bn_dh, nt_dh, bn_dw, nt_dw, splits;
-    size_t o_sidx, o_sp, o_H, o_valid, o_rowloss, o_big, o_part_dh, o_hT, total;
+    size_t o_sidx, o_sp, o_H, o_valid, o_rowloss, o_yk, o_big, o_part_dh, o_hT, total;
     size_t fwd_total;  // bytes the forward alone touches (a prefix of the workspace)
 };
 
@@ -327,7 +327,8 @@ bool make_plan(int64_t N, int d, int64_t V, int K, int chunk, Plan& P) {
     // partials at once, so its partials share the dh partials' place.  The
     // chunk's h transposed (for the dW GEMM) comes last.
     P.o_hT = P.o_big + dz + std::max(part_fwd, part_dh);
-    P.total = P.o_hT + align256(size_t(P.Cc) * d * 2);
+    P.o_yk = P.o_hT + align256(size_t(P.Cc) * d * 2);  // the one-call path: kept logits at the teacher ids
+    P.total = P.o_yk + align256(size_t(P.Cc) * K * 4);
     P.fwd_total = P.o_big + part_fwd;
     // the KL + cross-entropy mixture's forward keeps six partial arrays, not three
     P.total = std::max(P.total, P.o_big + 2 * part_fwd);
@@ -930,8 +931,9 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
         FKL_SMALL(KK_FWD_FINALIZE,
                   launch_fwd_finalize(pm, pl, pg, P.Cc, P.nt_v, rows, H, valid, T, lse + row0, rowloss + row0, s));
         // dz from the kept logits, in place (no second pass over the tensor cores)
-        FKL_SMALL(KK_FB_DZ, launch_dz_from_logits(yz, int64_t(P.Cc) * 64, V, pm, P.Cc, lse + row0, valid, n_valid, grad_loss, T,
-                                                  sidx, sp, K, rows, s));
+        FKL_SMALL(KK_FB_DZ, launch_dz_from_logits(yz, int64_t(P.Cc) * 64, V, pm, P.Cc, lse + row0, valid, n_valid,
+                                                  grad_loss, T, sidx, sp, K, rows,
+                                                  reinterpret_cast<float*>(w + P.o_yk), s));
         if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmHT_k, tmH_mn, tmW_mn, tmPart, tmDW, part,
                                           static_cast<char*>(dh) + size_t(row0) * d * 2, status, s))
             return st;

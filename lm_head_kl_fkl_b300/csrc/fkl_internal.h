@@ -141,7 +141,7 @@ void launch_or_flags(const int* flags, int n, int* out, cudaStream_t s);
 void launch_scale_grads(void* dh, size_t n_dh, float* dW, size_t n_dw, const float* g, int grid, cudaStream_t s);
 void launch_dz_from_logits(void* yz, int64_t pstride, int64_t V, const float* part_m, int part_stride,
                            const float* lse, const uint8_t* valid, const int* n_valid, const float* grad,
-                           float T, const int* sidx, const float* sp, int K, int rows, cudaStream_t s);
+                           float T, const int* sidx, const float* sp, int K, int rows, float* yk, cudaStream_t s);
 void launch_transpose_h(const void* h, int rows, int d, void* hT, int64_t ld, cudaStream_t s);
 
 }  // namespace fkl
