@@ -586,11 +586,11 @@ def run_fused(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x)
 
-    # ---- the smaller workloads (small LM head, Llama-8B->3.2B-like head) on the same call pair
+    # ---- the smaller workloads (tiny, small LM head, Llama-8B->3.2B-like head) on the same call pair
     legs = {}
     if not args.no_config_legs and args.config == 3 and args.shape is None and world == 1:
         del x
-        for cfg in (1, 2):
+        for cfg in (0, 1, 2):
             legs[f"config_{cfg}"] = config_leg(api, cfg, dev, stream, args.chunk, args.steps, args.warmup, peaks,
                                                peaks_kind, with_cpu=not args.no_cpu_baseline)
 
@@ -641,7 +641,7 @@ def main():
     ap.add_argument("--no-variants", action="store_true", help="skip the one-call forward+backward timing")
     ap.add_argument("--no-memory-stress", action="store_true", help="skip the N=131072 peak-memory leg")
     ap.add_argument("--no-config-legs", action="store_true",
-                    help="skip the small LM head and Llama-like head workloads (config_1, config_2 keys)")
+                    help="skip the tiny, small LM head and Llama-like head workloads (config_0..2 keys)")
     ap.add_argument("--shape", type=lambda s: tuple(int(v) for v in s.split(",")), default=None,
                     help="N,d,V,K: a smaller case of the chosen workload (profiling captures)")
     args = ap.parse_args()
