@@ -75,8 +75,9 @@ typedef enum {
  * fkl_forward_backward, fkl_mix_forward and fkl_mix_backward for these sizes
  * (chunk as passed to them).  Pure host arithmetic; 0 if the sizes are invalid.
  * It is O(chunk * V + N): one bf16 dz chunk buffer, split-K partials of dh for
- * one chunk, the sorted teacher cache of one chunk and 4 bytes per token
- * (1.79 GB at N = 131072, d = 2880, V = 201088, K = 100, default chunk). */
+ * one chunk, the chunk's h transposed, the sorted teacher cache of one chunk and
+ * 4 bytes per token (1.82 GB at N = 131072, d = 2880, V = 201088, K = 100,
+ * default chunk). */
 size_t fkl_workspace_size(int64_t N, int d, int64_t V, int K, int chunk);
 
 /* Forward: writes loss (one fp32, device) and lse[N] (fp32, natural-log
@@ -197,13 +198,15 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
  * lies in a tile whose max reaches it, so the candidates are gathered from the
  * per-tile lists -- completely, unless some such tile holds eight or more logits
  * >= theta; those rows (rare: eight of the row's top logits in one tile) get a
- * second tensor-core pass that keeps all their logits >= theta.  A last kernel
- * selects and sorts the K largest.  Where more than K logits tie at theta
- * itself, which of them are kept is unspecified.  The full N x V logits are
+ * second tensor-core pass over their 1024-row sub-chunk that keeps all their
+ * logits >= theta.  Selection and sorting of the K largest run one warp per row
+ * (a block per row for the rows of the second pass).  Where more than K logits
+ * tie at theta itself, which of them are kept is unspecified for the rows of the
+ * second pass (the others keep the smallest ids).  The full N x V logits are
  * never stored.  Conventions as above (device pointers, caller-owned,
- * stream-ordered, status word at the start of ws); chunk = 0 means 1024 rows.
- * The workspace is O(chunk * (min(V, 256 K) + V / 4)) bytes: 263 MB at
- * V = 201088, K = 100. */
+ * stream-ordered, status word at the start of ws); chunk = 0 means 4096 rows.
+ * The workspace is O(chunk * V / 4 + min(chunk, 1024) * min(V, 256 K)) bytes:
+ * 437 MB at V = 201088, K = 100. */
 size_t fkl_topk_workspace_size(int64_t N, int d, int64_t V, int K, int chunk);
 fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int64_t V, int K, int chunk,
                             int32_t* idx, float* logit, void* ws, size_t ws_bytes, void* stream);
