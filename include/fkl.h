@@ -206,7 +206,7 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
  * never stored.  Conventions as above (device pointers, caller-owned,
  * stream-ordered, status word at the start of ws); chunk = 0 means 4096 rows.
  * The workspace is O(chunk * V / 4 + min(chunk, 1024) * min(V, 256 K)) bytes:
- * 437 MB at V = 201088, K = 100. */
+ * 427 MB at V = 201088, K = 100. */
 size_t fkl_topk_workspace_size(int64_t N, int d, int64_t V, int K, int chunk);
 fkl_status fkl_teacher_topk(const void* h, const void* W, int64_t N, int d, int64_t V, int K, int chunk,
                             int32_t* idx, float* logit, void* ws, size_t ws_bytes, void* stream);
