@@ -341,6 +341,62 @@ def config_leg(api, cfg, dev, stream, chunk, steps, warmup, peaks, peaks_kind, w
     return out
 
 
+def dense_kl_step(h, W, idx, tlogit, mask, T):
+    """The dense method the pages compare the fused loss with: the full N x V logits
+    materialised (bf16 matmul, fp32 softmax over the vocabulary), the same top-K
+    forward KL, and autograd's backward through it.  A measurement baseline in plain
+    torch ops, not the library's path.  Returns (loss, dh, dW)."""
+    import torch
+    hh = h.detach().requires_grad_(True)
+    WW = W.detach().requires_grad_(True)
+    logq = torch.log_softmax((hh @ WW.t()).float() / T, dim=1)          # [N, V]
+    u = tlogit / T
+    finite = torch.isfinite(u)
+    logp = torch.log_softmax(torch.where(finite, u, torch.full_like(u, -float("inf"))), dim=1)
+    p = torch.where(finite, logp.exp(), torch.zeros_like(u))
+    plogp = torch.where(p > 0, p * logp, torch.zeros_like(u))
+    kl = (plogp - p * logq.gather(1, idx.long())).sum(dim=1)
+    valid = finite.any(dim=1)
+    if mask is not None:
+        valid = valid & (mask != 0)
+    n_valid = valid.sum()
+    loss = (T * T) * torch.where(valid, kl, torch.zeros_like(kl)).sum() / n_valid.clamp(min=1)
+    loss.backward()
+    return loss.detach(), hh.grad, WW.grad
+
+
+def dense_baseline(cfg, dev, steps=2):
+    """Peak device memory and time per step of dense_kl_step on a named workload."""
+    import torch
+    from lm_head_kl_fkl_b300 import synth
+    c = synth.CONFIGS[cfg]
+    x = synth.config_inputs(cfg)
+    h = torch.from_numpy(x["h"].view(np.int16)).view(torch.bfloat16).to(dev)
+    W = torch.from_numpy(x["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    idx, t, mask = (torch.from_numpy(x[k]).to(dev) for k in ("idx", "t", "mask"))
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    try:
+        dense_kl_step(h, W, idx, t, mask, c.T)  # warm-up (cuBLAS workspaces, allocator)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            loss, dh, dW = dense_kl_step(h, W, idx, t, mask, c.T)
+            del dh, dW
+        e1.record()
+        torch.cuda.synchronize()
+        out = {"workload": c.name, "N": c.N, "V": c.V, "d": c.d, "ms_per_step": e0.elapsed_time(e1) / steps,
+               "tokens_per_s": c.N / (e0.elapsed_time(e1) / steps / 1e3), "loss": float(loss.item()),
+               "peak_beyond_inputs_gb": (torch.cuda.max_memory_allocated(dev) - base) / 1e9}
+    except torch.cuda.OutOfMemoryError as e:
+        out = {"workload": c.name, "N": c.N, "V": c.V, "d": c.d, "out_of_memory": str(e).splitlines()[0]}
+    del h, W, idx, t, mask
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -599,6 +655,19 @@ def run_fused(args):
             legs[f"config_{cfg}"] = config_leg(api, cfg, dev, stream, args.chunk, args.steps, args.warmup, peaks,
                                                peaks_kind, with_cpu=not args.no_cpu_baseline)
 
+    # ---- the dense method (full N x V logits in plain torch) on the same workloads: its
+    # peak memory beside the fused path's (the pages' dense-versus-fused comparison)
+    dense = None
+    if not args.no_dense and args.config == 3 and args.shape is None and world == 1:
+        dense = {"what": "dense_kl_step: the N x V logits materialised (bf16 matmul, fp32 log-softmax), "
+                         "the same top-K forward KL, autograd backward; plain torch, a comparison baseline",
+                 "fused_config_3_peak_beyond_inputs_gb":
+                     (peak_mem - sum(a.numel() * a.element_size() for a in (h, W, idx, t, mask))) / 1e9,
+                 "fused_config_3_what": "the fused two-call path at the same workload: workspace, lse, loss, "
+                                        "dh (bf16) and dW (fp32)"}
+        for cfg in (1, 2, 3):
+            dense[f"config_{cfg}"] = dense_baseline(cfg, dev)
+
     # ---- the memory-stress workload (N = 131072): peak device memory of the same call pair
     mem = None
     ws_gb = ws.numel() / 1e9
@@ -624,6 +693,7 @@ def run_fused(args):
                 "resident_gb": base_mem / 1e9,
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
                 "variants": variants, "teacher_topk": topk, "memory_stress": mem, **legs,
+                "dense_baseline": dense,
                 "clocks": clk.summary(), "gpu_launches": launches, "device_status": status,
                 "kernel_digest": kernel_digest()}
         print(json.dumps(line), flush=True)
@@ -645,6 +715,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the one-call forward+backward timing")
     ap.add_argument("--no-memory-stress", action="store_true", help="skip the N=131072 peak-memory leg")
+    ap.add_argument("--no-dense", action="store_true",
+                    help="skip the dense (materialised N x V logits) comparison baseline")
     ap.add_argument("--no-config-legs", action="store_true",
                     help="skip the tiny, small LM head and Llama-like head workloads (config_0..2 keys)")
     ap.add_argument("--shape", type=lambda s: tuple(int(v) for v in s.split(",")), default=None,
