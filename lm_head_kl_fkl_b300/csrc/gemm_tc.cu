@@ -65,7 +65,11 @@
 //            max, y is exact to 2^-11 of |y| where q is largest.
 //
 // Operand majorness (template): K-major tiles arrive as one TMA box {64, rows};
-// MN-major tiles as boxes {64 (MN), 64 (K)} side by side, 8 KB apart.
+// MN-major tiles as boxes {64 (MN), 64 (K)} side by side, 8 KB apart.  When A is
+// the dz buffer (p.a_panel), it is read through a 3-D map of its 64-column panels
+// {64, rows, panel}: a K-major k-block is one box {64, 128, 1} (dh), an MN-major one
+// a single box {64, 64, 2} covering both panels of the CTA's 128 rows (dW); the
+// staged epilogues of dz and of the kept logits store into the same panels.
 #include <climits>
 #include <cmath>
 #include <mutex>
