@@ -606,6 +606,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tv[e] = -INFINITY;
                     ti[e] = INT_MAX;
                 }
+                // insert x (id xi) into the descending list, below the kept values >= x
+                auto insert = [&](float x, int xi) {
+                    bool gt[kTopPerTile];
+#pragma unroll
+                    for (int e = 0; e < kTopPerTile; ++e) gt[e] = x > tv[e];
+#pragma unroll
+                    for (int e = kTopPerTile - 1; e > 0; --e) {  // shift down below x's place
+                        tv[e] = gt[e - 1] ? tv[e - 1] : (gt[e] ? x : tv[e]);
+                        ti[e] = gt[e - 1] ? ti[e - 1] : (gt[e] ? xi : ti[e]);
+                    }
+                    tv[0] = gt[0] ? x : tv[0];
+                    ti[0] = gt[0] ? xi : ti[0];
+                };
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     const int col0 = v0 + c * 32;
@@ -614,20 +627,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     tmem_ld32(tt + c * 32, z);
                     const int nv = p.Ncols - col0;
+                    if (c == 0) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float x = (j < nv) ? z[j] : -INFINITY;
-                        const int xi = col0 + j;
-                        bool gt[kTopPerTile];
+                        for (int j = 0; j < 32; ++j) insert((j < nv) ? z[j] : -INFINITY, col0 + j);
+                    } else {
+                        // only the values above the current eighth can enter: each lane walks
+                        // its own mask in column order (most values of later chunks fail)
+                        uint32_t above = 0;
 #pragma unroll
-                        for (int e = 0; e < kTopPerTile; ++e) gt[e] = x > tv[e];
-#pragma unroll
-                        for (int e = kTopPerTile - 1; e > 0; --e) {  // shift down below x's place
-                            tv[e] = gt[e - 1] ? tv[e - 1] : (gt[e] ? x : tv[e]);
-                            ti[e] = gt[e - 1] ? ti[e - 1] : (gt[e] ? xi : ti[e]);
+                        for (int j = 0; j < 32; ++j) above |= (j < nv && z[j] > tv[kTopPerTile - 1]) ? (1u << j) : 0u;
+                        while (above) {
+                            const int j = __ffs(above) - 1;
+                            above &= above - 1;
+                            const float x = select32(z, j);
+                            if (x > tv[kTopPerTile - 1]) insert(x, col0 + j);
                         }
-                        tv[0] = gt[0] ? x : tv[0];
-                        ti[0] = gt[0] ? xi : ti[0];
                     }
                 }
                 tc_fence_before();
