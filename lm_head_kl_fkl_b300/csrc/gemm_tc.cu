@@ -468,35 +468,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (ylab >= col0 && ylab < col0 + 32) gy = select32(z, ylab - col0);
                     }
                     const int nv = p.Ncols - col0;
-                    float cm0 = -INFINITY, cm1 = -INFINITY;
+                    // the max of the raw logits (scale2 > 0: max(z) scale2 = max(z scale2), bit
+                    // for bit), then 2^(z scale2 - max) with one FMA per logit; columns beyond
+                    // Ncols (last tile only) are -inf
+                    if (nv < 32) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        z[j] = (j < nv) ? z[j] * p.scale2 : -INFINITY;
-                        z[j + 1] = (j + 1 < nv) ? z[j + 1] * p.scale2 : -INFINITY;
+                        for (int j = 0; j < 32; ++j) z[j] = (j < nv) ? z[j] : -INFINITY;
+                    }
+                    float cm0 = z[0], cm1 = z[1];
+#pragma unroll
+                    for (int j = 2; j < 32; j += 2) {
                         cm0 = fmaxf(cm0, z[j]);
                         cm1 = fmaxf(cm1, z[j + 1]);
                     }
-                    const float mnew = fmaxf(mrun, fmaxf(cm0, cm1));
+                    const float zmax = fmaxf(cm0, cm1);
+                    const float mnew = fmaxf(mrun, zmax * p.scale2);
+                    const float nm = -mnew;
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
-                        s0 += ex2_approx(z[j] - mnew);
-                        s1 += ex2_approx(z[j + 1] - mnew);
-                        s2 += ex2_approx(z[j + 2] - mnew);
-                        s3 += ex2_approx(z[j + 3] - mnew);
+                        s0 += ex2_approx(fmaf(z[j], p.scale2, nm));
+                        s1 += ex2_approx(fmaf(z[j + 1], p.scale2, nm));
+                        s2 += ex2_approx(fmaf(z[j + 2], p.scale2, nm));
+                        s3 += ex2_approx(fmaf(z[j + 3], p.scale2, nm));
                     }
                     lrun = lrun * ex2_approx(mrun - mnew) + ((s0 + s1) + (s2 + s3));
                     mrun = mnew;
-                    if constexpr (MIX) {  // the same online sum at temperature 1: z log2e = (z log2e / T) T
-                        float c1 = -INFINITY;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) c1 = fmaxf(c1, z[j] * p.T);
-                        const float m1new = fmaxf(m1run, c1);
+                    if constexpr (MIX) {  // the same online sum at temperature 1, on z log2e
+                        constexpr float kL2e = 1.4426950408889634f;
+                        const float m1new = fmaxf(m1run, zmax * kL2e);
+                        const float nm1 = -m1new;
                         float t0 = 0.f, t1 = 0.f;
 #pragma unroll
                         for (int j = 0; j < 32; j += 2) {
-                            t0 += ex2_approx(z[j] * p.T - m1new);
-                            t1 += ex2_approx(z[j + 1] * p.T - m1new);
+                            t0 += ex2_approx(fmaf(z[j], kL2e, nm1));
+                            t1 += ex2_approx(fmaf(z[j + 1], kL2e, nm1));
                         }
                         l1run = l1run * ex2_approx(m1run - m1new) + (t0 + t1);
                         m1run = m1new;
@@ -713,6 +719,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ylab = __ldg(p.label + row);
                     }
                 }
+                // coef 2^(z scale2 - lse2) = sign(coef) 2^(z scale2 - lse2 + log2|coef|): one FMA
+                // and one exponential per logit, the sign applied to the packed bf16 (coef = 0
+                // gives 2^-inf = 0)
+                const float bias = log2f(fabsf(coef)) - lse2, acoef = fabsf(coef);
+                const uint32_t sgn = coef < 0.f ? 0x80008000u : 0u;
                 if (!warp_wait(tfull0 + 8u * acc, aph, s_abort, p.status)) break;
                 tc_fence_after();
 #pragma unroll 1
@@ -731,17 +742,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int nv = p.Ncols - cc;
                         uint32_t w[16];
                         if constexpr (!MIX) {
+                            if (nv >= 32) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                z[j] = (j < nv) ? ex2_approx(z[j] * p.scale2 - lse2) : 0.f;
+                                for (int j = 0; j < 32; ++j) z[j] = ex2_approx(fmaf(z[j], p.scale2, bias));
+                            } else {  // the last tile: columns beyond Ncols are 0
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    z[j] = (j < nv) ? ex2_approx(fmaf(z[j], p.scale2, bias)) : 0.f;
+                            }
                             while (cur.next_id < cc + 32) {
                                 const int off = cur.next_id - cc;
+                                const float ps = acoef * cur.next_p;
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) z[j] -= (j == off) ? cur.next_p : 0.f;
+                                for (int j = 0; j < 32; ++j) z[j] -= (j == off) ? ps : 0.f;
                                 cur.advance();
                             }
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(coef * z[2 * j], coef * z[2 * j + 1]);
+                            for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(z[2 * j], z[2 * j + 1]) ^ sgn;
                         } else {
                             constexpr float kL2e = 1.4426950408889634f;
 #pragma unroll
