@@ -542,11 +542,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         cur.advance();
                     }
                     const int nv = p.Ncols - col0;
-                    float cm0 = -INFINITY, cm1 = -INFINITY;
+                    if (nv < 32) {  // the last tile: columns beyond Ncols are -inf
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        cm0 = fmaxf(cm0, (j < nv) ? z[j] : -INFINITY);
-                        cm1 = fmaxf(cm1, (j + 1 < nv) ? z[j + 1] : -INFINITY);
+                        for (int j = 0; j < 32; ++j) z[j] = (j < nv) ? z[j] : -INFINITY;
+                    }
+                    float cm0 = z[0], cm1 = z[1];
+#pragma unroll
+                    for (int j = 2; j < 32; j += 2) {
+                        cm0 = fmaxf(cm0, z[j]);
+                        cm1 = fmaxf(cm1, z[j + 1]);
                     }
                     mt = fmaxf(mt, fmaxf(cm0, cm1));
                 }
@@ -567,12 +571,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         __syncwarp();
                         tmem_ld32(tt + c2 * 64 + hh * 32, z);
                         const int nv = p.Ncols - cc;
+                        const float nmt = -mt;
+                        if (nv >= 32) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            z[j] = z[j] * p.scale2 - mt;
-                            z[j + 1] = z[j + 1] * p.scale2 - mt;
-                            l0 += (j < nv) ? ex2_approx(z[j]) : 0.f;
-                            l1 += (j + 1 < nv) ? ex2_approx(z[j + 1]) : 0.f;
+                            for (int j = 0; j < 32; j += 2) {
+                                z[j] = fmaf(z[j], p.scale2, nmt);
+                                z[j + 1] = fmaf(z[j + 1], p.scale2, nmt);
+                                l0 += ex2_approx(z[j]);
+                                l1 += ex2_approx(z[j + 1]);
+                            }
+                        } else {  // the last tile: columns beyond Ncols add nothing
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2) {
+                                z[j] = fmaf(z[j], p.scale2, nmt);
+                                z[j + 1] = fmaf(z[j + 1], p.scale2, nmt);
+                                l0 += (j < nv) ? ex2_approx(z[j]) : 0.f;
+                                l1 += (j + 1 < nv) ? ex2_approx(z[j + 1]) : 0.f;
+                            }
                         }
                         uint32_t w[16];
 #pragma unroll
