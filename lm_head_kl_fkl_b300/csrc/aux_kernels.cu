@@ -51,7 +51,9 @@ __global__ void teacher_prep_kernel(const int32_t* __restrict__ idx, const float
                                     int64_t V, float T, int* __restrict__ sidx, float* __restrict__ sp,
                                     float* __restrict__ H, uint8_t* __restrict__ valid,
                                     int* __restrict__ status) {
-    __shared__ int s_ix[4][kMaxK];
+    // per warp: sort keys (id, original position) and the probabilities by position
+    __shared__ unsigned long long s_key[4][kMaxK];
+    __shared__ float s_e[4][kMaxK];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 4 + w;
     if (r >= rows) return;
@@ -101,22 +103,36 @@ __global__ void teacher_prep_kernel(const int32_t* __restrict__ idx, const float
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
         const int k = lane + 32 * j;
-        if (k < K) s_ix[w][k] = ix[j];
-    }
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        const int k = lane + 32 * j;
         if (k < K) {
-            const int me = ix[j];
-            int rank = 0;
-            for (int i = 0; i < K; ++i) {
-                const int o = s_ix[w][i];
-                rank += (o < me) || (o == me && i < k);
-            }
-            sidx[static_cast<size_t>(r) * K + rank] = me;
-            sp[static_cast<size_t>(r) * K + rank] = e[j];
+            s_key[w][k] = (static_cast<unsigned long long>(static_cast<uint32_t>(ix[j])) << 32) | static_cast<uint32_t>(k);
+            s_e[w][k] = e[j];
         }
+    }
+    // ascending by id, equal ids by original position: a bitonic sort of the next
+    // power of two >= K slots (padding sorts last)
+    int P = 1;
+    while (P < K) P <<= 1;
+    for (int k = K + lane; k < P; k += 32) s_key[w][k] = ~0ull;
+    __syncwarp();
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int str = size >> 1; str > 0; str >>= 1) {
+            for (int i = lane; i < P; i += 32) {
+                const int j = i ^ str;
+                if (j > i) {
+                    const unsigned long long a = s_key[w][i], b = s_key[w][j];
+                    if ((a > b) == ((i & size) == 0)) {
+                        s_key[w][i] = b;
+                        s_key[w][j] = a;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    }
+    for (int k = lane; k < K; k += 32) {
+        const unsigned long long key = s_key[w][k];
+        sidx[static_cast<size_t>(r) * K + k] = static_cast<int>(key >> 32);
+        sp[static_cast<size_t>(r) * K + k] = s_e[w][static_cast<uint32_t>(key)];
     }
     if (lane == 0) {
         H[r] = hs;
@@ -125,10 +141,11 @@ __global__ void teacher_prep_kernel(const int32_t* __restrict__ idx, const float
 }
 
 // lse_i and KL_i of one chunk from the per-tile partials.  A block takes 8 rows;
-// 32 threads share a row, thread group g merging the tiles n = g, g + 32, ... (for
-// a fixed tile, the 8 rows are one 32-byte sector), and group 0 merges the 32
-// results in group order.  The order depends only on the tile index, so a row's
-// lse is the same whatever chunk it is in.
+// 32 threads share a row, thread group g merging the tiles n = g + 32 t (for a fixed
+// tile, the 8 rows are one 32-byte sector) into four independent running pairs by
+// t mod 4 (so that four loads and merges are in flight), then the four in order,
+// then the 32 groups pairwise in a fixed tree.  The order depends only on the tile
+// index, so a row's lse is the same whatever chunk it is in.
 constexpr int kFinRows = 8, kFinGroups = 32;
 
 __device__ __forceinline__ void merge_ml(float& M, float& L, float m, float l) {
@@ -141,6 +158,63 @@ __device__ __forceinline__ void merge_ml(float& M, float& L, float m, float l) {
     }
 }
 
+// A row's (max, sum, gather) over this thread's tiles n = grp + kFinGroups t, merged
+// into four independent pairs by t mod 4 and then in that order (the row's 32 groups
+// are merged afterwards by merge_groups).  The grouping depends only on n.
+struct MLG {
+    float M, L, G;
+};
+__device__ __forceinline__ MLG merge_tiles(const float* __restrict__ pm, const float* __restrict__ pl,
+                                           const float* __restrict__ pg, int stride, int ntiles, int grp, int r) {
+    float Ma[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, La[4] = {0.f, 0.f, 0.f, 0.f};
+    float Ga[4] = {0.f, 0.f, 0.f, 0.f};
+    int n = grp;
+    for (; n + 3 * kFinGroups < ntiles; n += 4 * kFinGroups) {
+        float m[4], l[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const size_t o = static_cast<size_t>(n + a * kFinGroups) * stride + r;
+            m[a] = pm[o];
+            l[a] = pl[o];
+            Ga[a] += pg[o];
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) merge_ml(Ma[a], La[a], m[a], l[a]);
+    }
+    for (int a = 0; n < ntiles; n += kFinGroups, ++a) {
+        const size_t o = static_cast<size_t>(n) * stride + r;
+        Ga[a] += pg[o];
+        merge_ml(Ma[a], La[a], pm[o], pl[o]);
+    }
+    MLG v{-INFINITY, 0.f, 0.f};
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        v.G += Ga[a];
+        merge_ml(v.M, v.L, Ma[a], La[a]);
+    }
+    return v;
+}
+
+// The row's 32 groups merged pairwise in a fixed tree through shared memory; every
+// thread of the block calls it (it synchronises), group 0 ends with the row's total.
+__device__ __forceinline__ void merge_groups(MLG& v, float (*sm)[kFinRows], float (*sl)[kFinRows],
+                                             float (*sg)[kFinRows], int grp, int rl) {
+    sm[grp][rl] = v.M;
+    sl[grp][rl] = v.L;
+    sg[grp][rl] = v.G;
+#pragma unroll
+    for (int half = kFinGroups / 2; half > 0; half >>= 1) {
+        __syncthreads();
+        if (grp < half) {
+            v.G += sg[grp + half][rl];
+            merge_ml(v.M, v.L, sm[grp + half][rl], sl[grp + half][rl]);
+            sm[grp][rl] = v.M;
+            sl[grp][rl] = v.L;
+            sg[grp][rl] = v.G;
+        }
+    }
+}
+
 __global__ void fwd_finalize_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                                     const float* __restrict__ pg, int stride, int ntiles, int rows,
                                     const float* __restrict__ H, const uint8_t* __restrict__ valid,
@@ -148,26 +222,13 @@ __global__ void fwd_finalize_kernel(const float* __restrict__ pm, const float* _
     __shared__ float s_m[kFinGroups][kFinRows], s_l[kFinGroups][kFinRows], s_g[kFinGroups][kFinRows];
     const int rl = threadIdx.x % kFinRows, grp = threadIdx.x / kFinRows;
     const int r = blockIdx.x * kFinRows + rl;
-    float M = -INFINITY, L = 0.f, G = 0.f;
-    if (r < rows) {
-        for (int n = grp; n < ntiles; n += kFinGroups) {
-            const size_t o = static_cast<size_t>(n) * stride + r;
-            G += pg[o];
-            merge_ml(M, L, pm[o], pl[o]);
-        }
-    }
-    s_m[grp][rl] = M;
-    s_l[grp][rl] = L;
-    s_g[grp][rl] = G;
-    __syncthreads();
+    MLG v{-INFINITY, 0.f, 0.f};
+    if (r < rows) v = merge_tiles(pm, pl, pg, stride, ntiles, grp, r);
+    merge_groups(v, s_m, s_l, s_g, grp, rl);
     if (grp != 0 || r >= rows) return;
-    for (int k = 1; k < kFinGroups; ++k) {
-        G += s_g[k][rl];
-        merge_ml(M, L, s_m[k][rl], s_l[k][rl]);
-    }
-    const float lse_r = (M + log2f(L)) * 0.69314718055994531f;
+    const float lse_r = (v.M + log2f(v.L)) * 0.69314718055994531f;
     lse[r] = lse_r;
-    rowloss[r] = valid[r] ? (H[r] - G / T + lse_r) : 0.f;
+    rowloss[r] = valid[r] ? (H[r] - v.G / T + lse_r) : 0.f;
 }
 
 // The same for the KL + hard-label cross-entropy mixture: also lse1_i (temperature
@@ -182,33 +243,19 @@ __global__ void fwd_finalize_mix_kernel(const float* __restrict__ pm, const floa
                                         int64_t V, float T, float alpha, float* __restrict__ lse,
                                         float* __restrict__ lse1, float* __restrict__ rowloss,
                                         int* __restrict__ status) {
-    __shared__ float s_v[6][kFinGroups][kFinRows];
+    __shared__ float s_v[3][kFinGroups][kFinRows];
     const int rl = threadIdx.x % kFinRows, grp = threadIdx.x / kFinRows;
     const int r = blockIdx.x * kFinRows + rl;
-    float M = -INFINITY, L = 0.f, G = 0.f, M1 = -INFINITY, L1 = 0.f, GY = 0.f;
+    MLG v{-INFINITY, 0.f, 0.f}, v1{-INFINITY, 0.f, 0.f};  // temperature T with the teacher gather; 1 with the label
     if (r < rows) {
-        for (int n = grp; n < ntiles; n += kFinGroups) {
-            const size_t o = static_cast<size_t>(n) * stride + r;
-            G += pg[o];
-            GY += pgy[o];
-            merge_ml(M, L, pm[o], pl[o]);
-            merge_ml(M1, L1, pm1[o], pl1[o]);
-        }
+        v = merge_tiles(pm, pl, pg, stride, ntiles, grp, r);
+        v1 = merge_tiles(pm1, pl1, pgy, stride, ntiles, grp, r);
     }
-    s_v[0][grp][rl] = M;
-    s_v[1][grp][rl] = L;
-    s_v[2][grp][rl] = G;
-    s_v[3][grp][rl] = M1;
-    s_v[4][grp][rl] = L1;
-    s_v[5][grp][rl] = GY;
+    merge_groups(v, s_v[0], s_v[1], s_v[2], grp, rl);
     __syncthreads();
+    merge_groups(v1, s_v[0], s_v[1], s_v[2], grp, rl);
     if (grp != 0 || r >= rows) return;
-    for (int k = 1; k < kFinGroups; ++k) {
-        G += s_v[2][k][rl];
-        GY += s_v[5][k][rl];
-        merge_ml(M, L, s_v[0][k][rl], s_v[1][k][rl]);
-        merge_ml(M1, L1, s_v[3][k][rl], s_v[4][k][rl]);
-    }
+    const float M = v.M, L = v.L, G = v.G, M1 = v1.M, L1 = v1.L, GY = v1.G;
     constexpr float kLn2 = 0.69314718055994531f;
     const float lse_r = (M + log2f(L)) * kLn2;
     const float lse1_r = (M1 + log2f(L1)) * kLn2;
