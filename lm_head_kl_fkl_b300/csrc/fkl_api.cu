@@ -462,7 +462,7 @@ constexpr auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 //   dW (+)= dz^T h_chunk (TMA store for chunk 0, reduce-add after; one owner per
 //   output tile, chunks in stream order).
 fkl_status grads_from_dz(const Plan& P, int64_t c, int rows, const CUtensorMap& tmDz_k, const CUtensorMap& tmDz_mn,
-                         const CUtensorMap& tmHT_k, const CUtensorMap& tmH_mn, const CUtensorMap& tmW_mn,
+                         const CUtensorMap& tmHT_k, const CUtensorMap& tmW_mn,
                          const CUtensorMap& tmPart, const CUtensorMap& tmDW, float* part, void* dh_chunk, int* status,
                          cudaStream_t s) {
     const int d = P.d;
@@ -493,8 +493,6 @@ fkl_status grads_from_dz(const Plan& P, int64_t c, int rows, const CUtensorMap& 
     r.Ncols = d;
     r.status = status;
     r.reduce = c > 0 ? 1 : 0;
-    if (getenv("FKL_DW_B_MN"))  // experiment: h as an MN-major operand
-        return run_gemm(KK_BWD_DW, P.bn_dw, 1, 1, EPI_F32, tmDz_mn, tmH_mn, tmDW, r, flop, s);
     return run_gemm(KK_BWD_DW, P.bn_dw, 1, 0, EPI_F32, tmDz_mn, tmHT_k, tmDW, r, flop, s);
 }
 
@@ -617,9 +615,8 @@ fkl_status backward_enqueue(const Plan& P, const void* h, const void* W, const i
         FKL_SMALL(KK_TEACHER_PREP,
                   launch_teacher_prep(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status, s));
         const char* hc = static_cast<const char*>(h) + size_t(row0) * d * 2;
-        CUtensorMap tmH_k, tmH_mn, tmHT_k, tmDz_st, tmDz_k, tmDz_mn, tmPart;
+        CUtensorMap tmH_k, tmHT_k, tmDz_st, tmDz_k, tmDz_mn, tmPart;
         FKL_TMAP(tmH_k, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 128);
-        FKL_TMAP(tmH_mn, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 64);
         // the dW GEMM's B operand: each CTA of a pair loads half of a (sub-)tile's columns of d
         FKL_TMAP(tmHT_k, BF16, hT, uint64_t(rows), uint64_t(d), uint64_t(P.Cc) * 2, 64,
                  uint32_t(std::min(P.bn_dw, 256) / 2));
@@ -657,7 +654,7 @@ fkl_status backward_enqueue(const Plan& P, const void* h, const void* W, const i
                                      flop, s))
             return st;
 
-        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmHT_k, tmH_mn, tmW_mn, tmPart, tmDW, part,
+        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmHT_k, tmW_mn, tmPart, tmDW, part,
                                           static_cast<char*>(dh) + size_t(row0) * d * 2, status, s))
             return st;
     }
@@ -895,9 +892,8 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
         FKL_SMALL(KK_TEACHER_PREP,
                   launch_teacher_prep(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status, s));
         const char* hc = static_cast<const char*>(h) + size_t(row0) * d * 2;
-        CUtensorMap tmH_k, tmH_mn, tmHT_k, tmY_st, tmDz_k, tmDz_mn, tmPart;
+        CUtensorMap tmH_k, tmHT_k, tmY_st, tmDz_k, tmDz_mn, tmPart;
         FKL_TMAP(tmH_k, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 128);
-        FKL_TMAP(tmH_mn, BF16, hc, uint64_t(d), uint64_t(rows), uint64_t(d) * 2, 64, 64);
         // the dW GEMM's B operand: each CTA of a pair loads half of a (sub-)tile's columns of d
         FKL_TMAP(tmHT_k, BF16, hT, uint64_t(rows), uint64_t(d), uint64_t(P.Cc) * 2, 64,
                  uint32_t(std::min(P.bn_dw, 256) / 2));
@@ -934,7 +930,7 @@ fkl_status fkl_forward_backward(const void* h, const void* W, const int32_t* idx
         FKL_SMALL(KK_FB_DZ, launch_dz_from_logits(yz, int64_t(P.Cc) * 64, V, pm, P.Cc, lse + row0, valid, n_valid,
                                                   grad_loss, T, sidx, sp, K, rows,
                                                   reinterpret_cast<float*>(w + P.o_yk), s));
-        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmHT_k, tmH_mn, tmW_mn, tmPart, tmDW, part,
+        if (fkl_status st = grads_from_dz(P, c, rows, tmDz_k, tmDz_mn, tmHT_k, tmW_mn, tmPart, tmDW, part,
                                           static_cast<char*>(dh) + size_t(row0) * d * 2, status, s))
             return st;
     }
