@@ -347,51 +347,91 @@ __global__ void teacher_y_kernel(const uint16_t* __restrict__ yz, int64_t pstrid
 constexpr int kDzRows = 64;    // rows per block of dz_panels_kernel
 constexpr int kDzPanels = 16;  // panels per block
 
+// 2^x with the special-function unit (relative error ~2^-22, results below 2^-126
+// flushed to zero): ample for a bf16 result.
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Eight fp16 y of one row -> eight bf16 dz = sign * 2^(y + shift), shift = m_tile +
+// log2|coef| - lse log2e (-inf for a row whose coef is 0); columns >= V (only in the
+// last panel) get 0.
+__device__ __forceinline__ uint4 dz_from_y8(uint4 in, float shift, uint32_t sgn, int64_t v, int64_t V) {
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+        const __nv_bfloat162 ab = __floats2bfloat162_rn(ex2_fast(y.x + shift), ex2_fast(y.y + shift));
+        o[j] = *reinterpret_cast<const uint32_t*>(&ab) ^ sgn;
+    }
+    if (v + 8 > V) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (v + 2 * j >= V) o[j] &= 0xffff0000u;
+            if (v + 2 * j + 1 >= V) o[j] &= 0x0000ffffu;
+        }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// A block covers 64 rows x kDzPanels panels; thread t owns columns (t % 8) * 8 .. + 7
+// of rows t / 8 and t / 8 + 32 in every panel, so it keeps its two rows' constants in
+// registers, and it loads the next panel's 16-byte pieces before converting the
+// current ones.
 __global__ void __launch_bounds__(256)
     dz_panels_kernel(uint16_t* __restrict__ yz, int64_t pstride, int64_t npan, int64_t V,
                      const float* __restrict__ part_m, int stride, const float* __restrict__ lse,
                      const uint8_t* __restrict__ valid, const int* __restrict__ n_valid, const float* __restrict__ grad,
                      float T, int rows) {
-    __shared__ float s_coef[kDzRows], s_lse2[kDzRows], s_shift[kDzRows];
     const int t = threadIdx.x;
     const int r0 = blockIdx.x * kDzRows;
     const int64_t p0 = static_cast<int64_t>(blockIdx.y) * kDzPanels;
-    if (t < kDzRows) {
-        DzRow d{0.f, 0.f};
-        if (r0 + t < rows) d = dz_row(lse, valid, n_valid, grad, T, r0 + t);
-        s_coef[t] = d.coef;
-        s_lse2[t] = d.lse2;
-    }
     const int64_t p1 = p0 + kDzPanels < npan ? p0 + kDzPanels : npan;
+    const int col = (t & 7) * 8;
+    int ra[2];
+    bool ok[2];
+    float bias[2], shift[2] = {0.f, 0.f};
+    uint32_t sgn[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        ra[i] = (t >> 3) + 32 * i;
+        ok[i] = r0 + ra[i] < rows;
+        bias[i] = -INFINITY;
+        sgn[i] = 0u;
+        if (ok[i]) {
+            const DzRow d = dz_row(lse, valid, n_valid, grad, T, r0 + ra[i]);
+            bias[i] = log2f(fabsf(d.coef)) - d.lse2;  // -inf when coef is 0
+            sgn[i] = d.coef < 0.f ? 0x80008000u : 0u;
+        }
+    }
+    auto piece = [&](int64_t p, int i) {
+        return reinterpret_cast<uint4*>(yz + p * pstride + static_cast<int64_t>(r0 + ra[i]) * 64 + col);
+    };
+    uint4 cur[2], nxt[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        cur[i] = nxt[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (ok[i]) cur[i] = *piece(p0, i);
+    }
     for (int64_t p = p0; p < p1; ++p) {
+        if (p + 1 < p1) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                if (ok[i]) nxt[i] = *piece(p + 1, i);
+        }
         if (p == p0 || (p & 3) == 0) {  // a 256-column tile spans four panels
-            __syncthreads();
-            if (t < kDzRows && r0 + t < rows)
-                s_shift[t] = part_m[static_cast<size_t>(p >> 2) * stride + r0 + t] - s_lse2[t];
-            __syncthreads();
-        }
-        uint16_t* base = yz + p * pstride + static_cast<int64_t>(r0) * 64;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int c = t + 256 * i;  // chunk of 8 columns: row c / 8, columns (c % 8) * 8 ...
-            const int row = c >> 3, col = (c & 7) * 8;
-            if (r0 + row >= rows) continue;
-            uint4* p8 = reinterpret_cast<uint4*>(base + row * 64 + col);
-            const uint4 in = *p8;
-            const float shift = s_shift[row], coef = s_coef[row];
-            const int64_t v = p * 64 + col;
-            const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-                const float a = (v + 2 * j < V) ? coef * exp2f(y.x + shift) : 0.f;
-                const float b = (v + 2 * j + 1 < V) ? coef * exp2f(y.y + shift) : 0.f;
-                const __nv_bfloat162 ab = __floats2bfloat162_rn(a, b);
-                o[j] = *reinterpret_cast<const uint32_t*>(&ab);
-            }
-            *p8 = make_uint4(o[0], o[1], o[2], o[3]);
+            for (int i = 0; i < 2; ++i)
+                if (ok[i]) shift[i] = part_m[static_cast<size_t>(p >> 2) * stride + r0 + ra[i]] + bias[i];
         }
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            if (ok[i]) *piece(p, i) = dz_from_y8(cur[i], shift[i], sgn[i], p * 64 + col, V);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) cur[i] = nxt[i];
     }
 }
 

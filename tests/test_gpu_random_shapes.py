@@ -57,3 +57,61 @@ def test_random_shape_two_call_and_one_call(case):
     one = dict(loss=float(loss.item()), lse=lse.cpu().numpy().astype(np.float64),
                dh=dh.float().cpu().numpy().astype(np.float64), dW=dW.cpu().numpy().astype(np.float64))
     _check(x, one, "one-call/")
+
+
+def _mix_shape(i):
+    rng = np.random.default_rng(13000 + i)
+    while True:
+        N = int(rng.integers(1, 1200))
+        d = 8 * int(rng.integers(1, 97))
+        V = int(rng.integers(8, 16000))
+        K = int(min(V, rng.integers(1, 257)))
+        if N * d * V <= 2e9:
+            break
+    T = float(np.exp(rng.uniform(np.log(0.5), np.log(4.0))))
+    chunk = int(rng.choice([0, 128, 256, 512]))
+    alpha = float(rng.choice([0.0, 0.25, 0.5, 0.9, 1.0]))
+    return N, d, V, K, T, chunk, alpha
+
+
+MIX_CASES = [_mix_shape(i) for i in range(6)]
+
+
+@pytest.mark.parametrize("case", MIX_CASES, ids=lambda c: "N{}_d{}_V{}_K{}_T{:.2f}_c{}_a{}".format(*c))
+def test_random_shape_mixture(case):
+    """The KL + hard-label cross-entropy mixture on seeded random shapes, labels and
+    alpha, against both fp64 oracles."""
+    from tests.test_gpu_mixture import _check as mix_check, _labels, _run_mix
+    N, d, V, K, T, chunk, alpha = case
+    x = synth.make_inputs(N, d, V, K, T, 0.05, "uniform", seed=13500 + N + V)
+    label = _labels(x, 13600 + N)
+    mix_check(x, label, alpha, _run_mix(to_device(x), label, alpha, chunk, grad=0.75), grad=0.75)
+
+
+def _topk_shape(i):
+    rng = np.random.default_rng(14000 + i)
+    while True:
+        N = int(rng.integers(1, 900))
+        d = 8 * int(rng.integers(1, 65))
+        V = int(rng.integers(1, 60000))
+        K = int(min(V, rng.integers(1, 257)))
+        if N * d * V <= 2e9:
+            break
+    chunk = int(rng.choice([0, 128, 256, 384]))
+    return N, d, V, K, chunk
+
+
+TOPK_CASES = [_topk_shape(i) for i in range(8)]
+
+
+@pytest.mark.parametrize("case", TOPK_CASES, ids=lambda c: "N{}_d{}_V{}_K{}_c{}".format(*c))
+def test_random_shape_teacher_topk(case):
+    """The teacher top-K cache producer on seeded random shapes and chunk sizes, checked
+    as the dedicated top-K tests check it: what is unique exactly, the rest for validity."""
+    from tests.test_gpu_teacher_topk import _bf16, _check as topk_check, _run
+    N, d, V, K, chunk = case
+    rng = np.random.default_rng(14500 + N + V)
+    h = _bf16(rng.standard_normal((N, d)))
+    W = _bf16(rng.standard_normal((V, d)) / np.sqrt(d))
+    idx, val = _run(h, W, K, chunk)
+    topk_check(h, W, K, idx, val)
