@@ -43,30 +43,64 @@ __global__ void count_valid_kernel(const float* __restrict__ t, const uint8_t* _
     if (threadIdx.x == 0 && s_cnt) atomicAdd(n_valid, s_cnt);
 }
 
+// Ascending bitonic sort of 32 E keys held by one warp, key i = lane + 32 j in
+// v[j] of lane `lane`: compare-exchanges at a distance below 32 go through warp
+// shuffles, the others stay inside a lane's registers.
+template <int E>
+__device__ __forceinline__ void warp_bitonic_sort(unsigned long long (&v)[E], int lane) {
+    constexpr int P = 32 * E;
+#pragma unroll
+    for (int size = 2; size <= P; size <<= 1) {
+#pragma unroll
+        for (int str = size >> 1; str > 0; str >>= 1) {
+            if (str >= 32) {
+                const int js = str >> 5;
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    if (j & js) continue;
+                    const bool asc = ((32 * j) & size) == 0;  // size >= 64: the lane does not matter
+                    const unsigned long long a = v[j], b = v[j | js];
+                    const bool sw = (a > b) == asc;
+                    v[j] = sw ? b : a;
+                    v[j | js] = sw ? a : b;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[j], str);
+                    const bool asc = ((lane + 32 * j) & size) == 0;
+                    const bool keep_min = ((lane & str) == 0) == asc;
+                    v[j] = keep_min ? (o < v[j] ? o : v[j]) : (o > v[j] ? o : v[j]);
+                }
+            }
+        }
+    }
+}
+
 // Per row of a chunk (one warp per row): p = softmax(t/T) over the K cached
-// entries, H = sum p log p, validity, and (id, p) sorted by id.  Ids outside
-// [0, V) raise FKL_ERR_INDEX and are replaced by INT_MAX, which no tile reaches.
+// entries, H = sum p log p, validity, and (id, p) sorted by id (equal ids by their
+// position in the cache).  Ids outside [0, V) raise FKL_ERR_INDEX and are replaced by
+// INT_MAX, which no tile reaches.  E = ceil(K / 32) rounded up to a power of two:
+// each lane holds E entries, entry k = lane + 32 j in slot j.
+template <int E>
 __global__ void teacher_prep_kernel(const int32_t* __restrict__ idx, const float* __restrict__ t,
                                     const uint8_t* __restrict__ mask, int64_t row0, int rows, int K,
                                     int64_t V, float T, int* __restrict__ sidx, float* __restrict__ sp,
                                     float* __restrict__ H, uint8_t* __restrict__ valid,
                                     int* __restrict__ status) {
-    // per warp: sort keys (id, original position) and the probabilities by position
-    __shared__ unsigned long long s_key[4][kMaxK];
-    __shared__ float s_e[4][kMaxK];
+    __shared__ float s_e[4][32 * E];  // p by original position
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 4 + w;
     if (r >= rows) return;
     const int64_t gr = row0 + r;
     const int32_t* ir = idx + gr * K;
     const float* tr = t + gr * K;
-    constexpr int PER = kMaxK / 32;
-    int ix[PER];
-    float u[PER];
+    int ix[E];
+    float u[E];
     float mx = -INFINITY;
     bool bad = false;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
+    for (int j = 0; j < E; ++j) {
         const int k = lane + 32 * j;
         ix[j] = INT_MAX;
         u[j] = -INFINITY;
@@ -85,54 +119,36 @@ __global__ void teacher_prep_kernel(const int32_t* __restrict__ idx, const float
     if (bad) atomicCAS(status, 0, static_cast<int>(FKL_ERR_INDEX));
     mx = warp_max(mx);
     const bool has_mass = mx > -INFINITY;
-    float e[PER];
+    float e[E];
     float s = 0.f;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
+    for (int j = 0; j < E; ++j) {
         e[j] = (has_mass && u[j] > -INFINITY) ? expf(u[j] - mx) : 0.f;
         s += e[j];
     }
     s = warp_sum(s);
     float hs = 0.f;
+    unsigned long long key[E];
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
+    for (int j = 0; j < E; ++j) {
+        const int k = lane + 32 * j;
         e[j] = has_mass ? e[j] / s : 0.f;
         if (e[j] > 0.f) hs += e[j] * logf(e[j]);
+        s_e[w][k] = e[j];
+        // ascending by id, equal ids by position; slots beyond K sort last
+        key[j] = k < K ? (static_cast<unsigned long long>(static_cast<uint32_t>(ix[j])) << 32) | static_cast<uint32_t>(k)
+                       : ~0ull;
     }
     hs = warp_sum(hs);
+    warp_bitonic_sort<E>(key, lane);
+    __syncwarp();
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
+    for (int j = 0; j < E; ++j) {
         const int k = lane + 32 * j;
         if (k < K) {
-            s_key[w][k] = (static_cast<unsigned long long>(static_cast<uint32_t>(ix[j])) << 32) | static_cast<uint32_t>(k);
-            s_e[w][k] = e[j];
+            sidx[static_cast<size_t>(r) * K + k] = static_cast<int>(key[j] >> 32);
+            sp[static_cast<size_t>(r) * K + k] = s_e[w][static_cast<uint32_t>(key[j])];
         }
-    }
-    // ascending by id, equal ids by original position: a bitonic sort of the next
-    // power of two >= K slots (padding sorts last)
-    int P = 1;
-    while (P < K) P <<= 1;
-    for (int k = K + lane; k < P; k += 32) s_key[w][k] = ~0ull;
-    __syncwarp();
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int str = size >> 1; str > 0; str >>= 1) {
-            for (int i = lane; i < P; i += 32) {
-                const int j = i ^ str;
-                if (j > i) {
-                    const unsigned long long a = s_key[w][i], b = s_key[w][j];
-                    if ((a > b) == ((i & size) == 0)) {
-                        s_key[w][i] = b;
-                        s_key[w][j] = a;
-                    }
-                }
-            }
-            __syncwarp();
-        }
-    }
-    for (int k = lane; k < K; k += 32) {
-        const unsigned long long key = s_key[w][k];
-        sidx[static_cast<size_t>(r) * K + k] = static_cast<int>(key >> 32);
-        sp[static_cast<size_t>(r) * K + k] = s_e[w][static_cast<uint32_t>(key)];
     }
     if (lane == 0) {
         H[r] = hs;
@@ -518,19 +534,50 @@ __device__ __forceinline__ int warp_sum(int c) {
     return c;
 }
 
+// Candidates of one row, (key, id) pairs in shared memory, sorted by key
+// descending and id ascending (one ascending sort of (~key, id) as a 64-bit value,
+// in registers: E slots per lane, 32 E >= n); the first K are written out.
+template <int E>
+__device__ __forceinline__ void sort_and_write(const uint32_t* skey, const int* sid, int n, int K, int lane,
+                                               int32_t* __restrict__ idx_row, float* __restrict__ logit_row) {
+    unsigned long long c[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        const int i = lane + 32 * j;
+        c[j] = i < n ? (static_cast<unsigned long long>(~skey[i]) << 32) | static_cast<uint32_t>(sid[i]) : ~0ull;
+    }
+    warp_bitonic_sort<E>(c, lane);
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        const int i = lane + 32 * j;
+        if (i < K) {
+            idx_row[i] = static_cast<int>(static_cast<uint32_t>(c[j]));
+            logit_row[i] = unkey(~static_cast<uint32_t>(c[j] >> 32));
+        }
+    }
+}
+
+// The rare rows with more than 256 candidates: the same in a function of its own,
+// so that its 16 slots per lane do not raise the register count of the common path.
+__device__ __noinline__ void sort_and_write_16(const uint32_t* skey, const int* sid, int n, int K, int lane,
+                                               int32_t* __restrict__ idx_row, float* __restrict__ logit_row) {
+    sort_and_write<16>(skey, sid, n, K, lane, idx_row, logit_row);
+}
+
 // Teacher top-K of one row per warp, from the first tensor-core pass's per-tile
 // top eight (tile maxima part_m [tile][row], kept logits and ids [tile][row][8]):
 //  1. theta = the K-th largest of the row's tile maxima (-inf with fewer than K
-//     tiles), by a bitwise search over order-preserving keys held in registers.
-//     At least K logits of the row are >= theta (each of the K tiles contributes
-//     its max), and every logit > theta lies in one of the < K tiles whose max
-//     exceeds theta.
+//     tiles), by a bitwise search over order-preserving keys held in registers
+//     (NK per lane), from the highest bit in which the keys differ.  At least K
+//     logits of the row are >= theta (each of the K tiles contributes its max), and
+//     every logit > theta lies in one of the < K tiles whose max exceeds theta.
 //  2. The tiles whose max reaches theta, listed in shared memory from the same
 //     registers; their kept logits are read 32 tiles at a time, and every kept
 //     logit > theta and up to K logits == theta are compacted, in tile order,
 //     into shared memory.
-//  3. The K largest (ties at the K-th value by the smallest ids), sorted by value
-//     descending and id ascending, written out.
+//  3. The candidates (those > theta; when fewer than K, with the first K - n_gt
+//     logits == theta, i.e. the smallest ids, appended) sorted by value descending and
+//     id ascending; the first K are the row's top K (ties by the smallest ids).
 // A tile whose eighth kept logit is still >= theta may hold more candidates than
 // were kept; such a row (or one with more than kTopCap candidates or kTopHits
 // tiles) is flagged instead -- theta stored, its counters cleared, its sub-chunk's
@@ -538,10 +585,10 @@ __device__ __forceinline__ int warp_sum(int c) {
 // topk_select_kernel.
 constexpr int kRowsPerBlock = 8;  // one warp per row
 constexpr int kTopCap = 384;      // candidates > theta held in shared memory per row
-constexpr int kTopHits = 2 * kMaxK;  // tiles reaching theta listed per row (aliases the selection slots)
-constexpr int kThKeys = 32;       // tile maxima per lane kept in registers (more are re-read)
+constexpr int kTopHits = 2 * kMaxK;  // tiles reaching theta listed per row
 
-__global__ void __launch_bounds__(32 * kRowsPerBlock)
+template <int NK>  // tile maxima per lane kept in registers; tiles beyond 32 NK are re-read
+__global__ void __launch_bounds__(32 * kRowsPerBlock, 4)
     topk_rows_kernel(const float* __restrict__ part_m, const float* __restrict__ top_v,
                      const int* __restrict__ top_i, int stride, int ntiles, int rows, int K, int sub_rows,
                      float* __restrict__ theta, int* __restrict__ cnt_gt, int* __restrict__ cnt_eq,
@@ -550,34 +597,48 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
     __shared__ uint32_t s_key[kRowsPerBlock][kTopCap];
     __shared__ int s_id[kRowsPerBlock][kTopCap];
     __shared__ int s_tie[kRowsPerBlock][kMaxK];
-    // per warp: the selection's keys [0, kMaxK) and ids [kMaxK, 2 kMaxK); the tile list before it
-    __shared__ uint32_t s_sel[kRowsPerBlock][2 * kMaxK];
-    static_assert(kTopHits <= 2 * kMaxK, "the tile list fits the selection slots");
+    __shared__ int s_hits[kRowsPerBlock][kTopHits];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    uint32_t* const s_skey = s_sel[w];
-    int* const s_sid = reinterpret_cast<int*>(s_sel[w] + kMaxK);
-    int* const s_hit = reinterpret_cast<int*>(s_sel[w]);
+    int* const s_hit = s_hits[w];
     const int r = blockIdx.x * kRowsPerBlock + w;
     if (r >= rows) return;  // whole warps only; no block-wide barrier follows
     const unsigned lt = (1u << lane) - 1u;
 
     // 1. theta
-    uint32_t key[kThKeys];
+    uint32_t key[NK];
+    uint32_t k_and = ~0u, k_or = 0u;  // over the row's keys: their common leading bits
 #pragma unroll
-    for (int j = 0; j < kThKeys; ++j) {
+    for (int j = 0; j < NK; ++j) {
         const int n = lane + 32 * j;
-        key[j] = n < ntiles ? fkey(part_m[static_cast<size_t>(n) * stride + r]) : 0u;
+        key[j] = 0u;
+        if (n < ntiles) {
+            key[j] = fkey(part_m[static_cast<size_t>(n) * stride + r]);
+            k_and &= key[j];
+            k_or |= key[j];
+        }
     }
+    for (int n = lane + 32 * NK; n < ntiles; n += 32) {
+        const uint32_t kk = fkey(part_m[static_cast<size_t>(n) * stride + r]);
+        k_and &= kk;
+        k_or |= kk;
+    }
+    k_and = __reduce_and_sync(0xffffffffu, k_and);
+    k_or = __reduce_or_sync(0xffffffffu, k_or);
     uint32_t t = 0;  // largest key with at least K tile maxima at or above it
     if (ntiles >= K) {
-        for (int b = 31; b >= 0; --b) {
+        // every key shares the bits above the highest one in which two keys differ,
+        // and so does theta: the search starts below them
+        const uint32_t diff = k_and ^ k_or;
+        const int hb = diff ? 31 - __clz(diff) : -1;
+        t = hb < 0 ? k_and : hb >= 31 ? 0u : (k_and & ~((2u << hb) - 1u));  // hb < 0: all keys are equal
+        for (int b = hb; b >= 0; --b) {
             const uint32_t cand = t | (1u << b);
             int c = 0;
 #pragma unroll
-            for (int j = 0; j < kThKeys; ++j) c += key[j] >= cand;
-            for (int n = lane + 32 * kThKeys; n < ntiles; n += 32)
+            for (int j = 0; j < NK; ++j) c += key[j] >= cand;
+            for (int n = lane + 32 * NK; n < ntiles; n += 32)
                 c += fkey(part_m[static_cast<size_t>(n) * stride + r]) >= cand;
-            if (warp_sum(c) >= K) t = cand;
+            if (static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c))) >= K) t = cand;
         }
     }
     const float th = ntiles >= K ? unkey(t) : -INFINITY;
@@ -586,14 +647,14 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
     // 2. the tiles reaching theta, then their kept logits
     int n_hit = 0;
 #pragma unroll
-    for (int j = 0; j < kThKeys; ++j) {
+    for (int j = 0; j < NK; ++j) {
         const int n = lane + 32 * j;
         const bool hit = n < ntiles && key[j] >= tkey;
         const unsigned m = __ballot_sync(0xffffffffu, hit);
         if (hit && n_hit + __popc(m & lt) < kTopHits) s_hit[n_hit + __popc(m & lt)] = n;
         n_hit += __popc(m);
     }
-    for (int n0 = 32 * kThKeys; n0 < ntiles; n0 += 32) {
+    for (int n0 = 32 * NK; n0 < ntiles; n0 += 32) {
         const int n = n0 + lane;
         const bool hit = n < ntiles && fkey(part_m[static_cast<size_t>(n) * stride + r]) >= tkey;
         const unsigned m = __ballot_sync(0xffffffffu, hit);
@@ -657,98 +718,25 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
         return;
     }
     if (lane == 0) row_flag[r] = 0;
-    __syncwarp();
 
-    // 3. selection into s_skey / s_sid [0, K), then the sort
-    if (n_gt >= K) {
-        uint32_t tk = 0;  // key of the K-th largest candidate
-        for (int b = 31; b >= 0; --b) {
-            const uint32_t cand = tk | (1u << b);
-            int c = 0;
-            for (int i = lane; i < n_gt; i += 32) c += s_key[w][i] >= cand;
-            if (warp_sum(c) >= K) tk = cand;
-        }
-        int above = 0, at = 0;
-        for (int i = lane; i < n_gt; i += 32) {
-            above += s_key[w][i] > tk;
-            at += s_key[w][i] == tk;
-        }
-        above = warp_sum(above);
-        at = warp_sum(at);
-        const int need = K - above;  // candidates at the K-th value to keep, smallest ids first
-        uint32_t cut = 0x7fffffffu;  // keep the ties with id <= cut
-        if (at > need) {
-            cut = 0;
-            for (int b = 30; b >= 0; --b) {
-                const uint32_t c2 = cut | (1u << b);
-                int c = 0;
-                for (int i = lane; i < n_gt; i += 32)
-                    c += s_key[w][i] == tk && static_cast<uint32_t>(s_id[w][i]) < c2;
-                if (warp_sum(c) < need) cut = c2;
-            }
-        }
-        int m = 0;
-        const int nr = (n_gt + 31) & ~31;
-        for (int i0 = 0; i0 < nr; i0 += 32) {
-            const int i = i0 + lane;
-            bool keep = false;
-            uint32_t kk = 0;
-            int ii = 0;
-            if (i < n_gt) {
-                kk = s_key[w][i];
-                ii = s_id[w][i];
-                keep = kk > tk || (kk == tk && static_cast<uint32_t>(ii) <= cut);
-            }
-            const unsigned mk = __ballot_sync(0xffffffffu, keep);
-            if (keep) {
-                const int slot = m + __popc(mk & lt);
-                s_skey[slot] = kk;
-                s_sid[slot] = ii;
-            }
-            m += __popc(mk);
-        }
-    } else {
-        for (int i = lane; i < n_gt; i += 32) {
-            s_skey[i] = s_key[w][i];
-            s_sid[i] = s_id[w][i];
-        }
+    // 3. the candidates, completed with ties at theta when fewer than K, sorted
+    int n = n_gt;
+    if (n_gt < K) {
+        __syncwarp();
         for (int i = lane; i < K - n_gt; i += 32) {  // at least K - n_gt ties exist (K tiles reach theta)
-            s_skey[n_gt + i] = tkey;
-            s_sid[n_gt + i] = s_tie[w][i];
+            s_key[w][n_gt + i] = tkey;
+            s_id[w][n_gt + i] = s_tie[w][i];
         }
-    }
-    int P = 1;
-    while (P < K) P <<= 1;
-    for (int i = K + lane; i < P; i += 32) {
-        s_skey[i] = 0u;  // below every real key: sorts last
-        s_sid[i] = INT_MAX;
+        n = K;
     }
     __syncwarp();
-    // bitonic sort of the P slots: key descending, id ascending
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int str = size >> 1; str > 0; str >>= 1) {
-            for (int i = lane; i < P; i += 32) {
-                const int j = i ^ str;
-                if (j > i) {
-                    const bool desc = (i & size) == 0;
-                    const uint32_t ki = s_skey[i], kj = s_skey[j];
-                    const int ii = s_sid[i], ij = s_sid[j];
-                    const bool i_first = ki > kj || (ki == kj && ii < ij);
-                    if (i_first != desc) {
-                        s_skey[i] = kj;
-                        s_skey[j] = ki;
-                        s_sid[i] = ij;
-                        s_sid[j] = ii;
-                    }
-                }
-            }
-            __syncwarp();
-        }
-    }
-    for (int k = lane; k < K; k += 32) {
-        idx_out[static_cast<size_t>(r) * K + k] = s_sid[k];
-        logit_out[static_cast<size_t>(r) * K + k] = unkey(s_skey[k]);
-    }
+    int32_t* const idx_row = idx_out + static_cast<size_t>(r) * K;
+    float* const logit_row = logit_out + static_cast<size_t>(r) * K;
+    if (n <= 32) sort_and_write<1>(s_key[w], s_id[w], n, K, lane, idx_row, logit_row);
+    else if (n <= 64) sort_and_write<2>(s_key[w], s_id[w], n, K, lane, idx_row, logit_row);
+    else if (n <= 128) sort_and_write<4>(s_key[w], s_id[w], n, K, lane, idx_row, logit_row);
+    else if (n <= 256) sort_and_write<8>(s_key[w], s_id[w], n, K, lane, idx_row, logit_row);
+    else sort_and_write_16(s_key[w], s_id[w], n, K, lane, idx_row, logit_row);
 }
 
 // Per row (one block of 256): the K largest logits among the candidates, sorted by
@@ -873,9 +861,17 @@ void launch_topk_select(const float* cand_v, const int* cand_i, int cap, const i
 void launch_topk_rows(const float* part_m, const float* top_v, const int* top_i, int part_stride, int ntiles,
                       int rows, int K, int sub_rows, float* theta, int* cnt_gt, int* cnt_eq, uint8_t* row_flag,
                       int* sub_flag, int32_t* idx_out, float* logit_out, cudaStream_t s) {
-    topk_rows_kernel<<<(rows + kRowsPerBlock - 1) / kRowsPerBlock, 32 * kRowsPerBlock, 0, s>>>(
-        part_m, top_v, top_i, part_stride, ntiles, rows, K, sub_rows, theta, cnt_gt, cnt_eq, row_flag, sub_flag,
-        idx_out, logit_out);
+    const unsigned grid = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock);
+#define FKL_TOPK_ROWS(NK_)                                                                                     \
+    topk_rows_kernel<NK_><<<grid, 32 * kRowsPerBlock, 0, s>>>(part_m, top_v, top_i, part_stride, ntiles, rows, K, \
+                                                              sub_rows, theta, cnt_gt, cnt_eq, row_flag, sub_flag,  \
+                                                              idx_out, logit_out)
+    if (ntiles <= 32 * 4) FKL_TOPK_ROWS(4);
+    else if (ntiles <= 32 * 8) FKL_TOPK_ROWS(8);
+    else if (ntiles <= 32 * 16) FKL_TOPK_ROWS(16);
+    else if (ntiles <= 32 * 25) FKL_TOPK_ROWS(25);  // up to V = 204800 (e.g. 201088)
+    else FKL_TOPK_ROWS(32);
+#undef FKL_TOPK_ROWS
 }
 
 // *out |= any of flags[0, n): the teacher top-K call's record that some row took
@@ -924,8 +920,15 @@ void launch_count_valid(const float* tlogit, const uint8_t* mask, int64_t N, int
 void launch_teacher_prep(const int32_t* idx, const float* tlogit, const uint8_t* mask, int64_t row0,
                          int rows, int K, int64_t V, float T, int* sidx, float* sp, float* H,
                          uint8_t* valid, int* status, cudaStream_t s) {
-    teacher_prep_kernel<<<(rows + 3) / 4, 128, 0, s>>>(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H,
-                                                       valid, status);
+    const unsigned grid = static_cast<unsigned>((rows + 3) / 4);
+    if (K <= 32)
+        teacher_prep_kernel<1><<<grid, 128, 0, s>>>(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status);
+    else if (K <= 64)
+        teacher_prep_kernel<2><<<grid, 128, 0, s>>>(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status);
+    else if (K <= 128)
+        teacher_prep_kernel<4><<<grid, 128, 0, s>>>(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status);
+    else
+        teacher_prep_kernel<8><<<grid, 128, 0, s>>>(idx, tlogit, mask, row0, rows, K, V, T, sidx, sp, H, valid, status);
 }
 
 void launch_fwd_finalize(const float* pm, const float* pl, const float* pg, int stride, int ntiles,
