@@ -145,9 +145,10 @@ def forward(h, W, idx, tlogit, mask=None, T: float = 1.0, chunk: int = 0,
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     _expect_out(lse, "lse", torch.float32, (N,), dev)
-    st = _lib.lib().fkl_forward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
-                                float(T), int(chunk), _ptr(loss), _ptr(lse), _ptr(ws), ws_bytes,
-                                _stream(dev))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        st = _lib.lib().fkl_forward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
+                                    float(T), int(chunk), _ptr(loss), _ptr(lse), _ptr(ws), ws_bytes,
+                                    _stream(dev))
     _check(st, "fkl_forward")
     return loss, lse
 
@@ -164,9 +165,10 @@ def backward(h, W, idx, tlogit, mask, T: float, lse: torch.Tensor,
         ws = alloc_workspace(N, d, V, K, chunk, dev)
     ws_bytes = _ws_bytes(ws, dev)
     dh, dW = _grad_outputs(dh, dW, N, d, V, dev)
-    st = _lib.lib().fkl_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
-                                 float(T), int(chunk), _ptr(lse), _ptr(grad_loss), _ptr(dh),
-                                 _ptr(dW), _ptr(ws), ws_bytes, _stream(dev))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        st = _lib.lib().fkl_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
+                                     float(T), int(chunk), _ptr(lse), _ptr(grad_loss), _ptr(dh),
+                                     _ptr(dW), _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "fkl_backward")
     return dh, dW
 
@@ -182,9 +184,10 @@ def mix_forward(h, W, idx, tlogit, mask, label, T: float, alpha: float, chunk: i
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     lse1 = torch.empty(N, dtype=torch.float32, device=dev)
-    st = _lib.lib().fkl_mix_forward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), _ptr(label), N, d, V,
-                                    K, float(T), float(alpha), int(chunk), _ptr(loss), _ptr(lse), _ptr(lse1),
-                                    _ptr(ws), ws_bytes, _stream(dev))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        st = _lib.lib().fkl_mix_forward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), _ptr(label), N, d, V,
+                                        K, float(T), float(alpha), int(chunk), _ptr(loss), _ptr(lse), _ptr(lse1),
+                                        _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "fkl_mix_forward")
     return loss, lse, lse1
 
@@ -201,9 +204,10 @@ def mix_backward(h, W, idx, tlogit, mask, label, T: float, alpha: float, lse, ls
         ws = alloc_workspace(N, d, V, K, chunk, dev)
     ws_bytes = _ws_bytes(ws, dev)
     dh, dW = _grad_outputs(None, None, N, d, V, dev)
-    st = _lib.lib().fkl_mix_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), _ptr(label), N, d,
-                                     V, K, float(T), float(alpha), int(chunk), _ptr(lse), _ptr(lse1),
-                                     _ptr(grad_loss), _ptr(dh), _ptr(dW), _ptr(ws), ws_bytes, _stream(dev))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        st = _lib.lib().fkl_mix_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), _ptr(label), N, d,
+                                         V, K, float(T), float(alpha), int(chunk), _ptr(lse), _ptr(lse1),
+                                         _ptr(grad_loss), _ptr(dh), _ptr(dW), _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "fkl_mix_backward")
     return dh, dW
 
@@ -227,9 +231,10 @@ def forward_backward(h, W, idx, tlogit, mask, T: float, grad_loss: Optional[torc
         lse = torch.empty(N, dtype=torch.float32, device=dev)
     _expect_out(lse, "lse", torch.float32, (N,), dev)
     dh, dW = _grad_outputs(dh, dW, N, d, V, dev)
-    st = _lib.lib().fkl_forward_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
-                                         float(T), int(chunk), _ptr(grad_loss), _ptr(loss), _ptr(lse),
-                                         _ptr(dh), _ptr(dW), _ptr(ws), ws_bytes, _stream(dev))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        st = _lib.lib().fkl_forward_backward(_ptr(h), _ptr(W), _ptr(idx), _ptr(tlogit), _ptr(mask), N, d, V, K,
+                                             float(T), int(chunk), _ptr(grad_loss), _ptr(loss), _ptr(lse),
+                                             _ptr(dh), _ptr(dW), _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "fkl_forward_backward")
     return loss, lse, dh, dW
 
@@ -257,15 +262,17 @@ def teacher_topk(h: torch.Tensor, W: torch.Tensor, K: int, chunk: int = 0,
     ws_bytes = _ws_bytes(ws, dev)
     idx = torch.empty((N, K), dtype=torch.int32, device=dev)
     logit = torch.empty((N, K), dtype=torch.float32, device=dev)
-    st = L.fkl_teacher_topk(_ptr(h), _ptr(W), N, d, V, int(K), int(chunk), _ptr(idx), _ptr(logit), _ptr(ws),
-                            ws_bytes, _stream(dev))
+    with torch.cuda.device(dev):  # the library launches on the current device
+        st = L.fkl_teacher_topk(_ptr(h), _ptr(W), N, d, V, int(K), int(chunk), _ptr(idx), _ptr(logit), _ptr(ws),
+                                ws_bytes, _stream(dev))
     _check(st, "fkl_teacher_topk")
     return idx, logit
 
 
 def get_status(ws: torch.Tensor) -> int:
     """Synchronises the current stream and returns the workspace's device status word."""
-    return int(_lib.lib().fkl_get_status(_ptr(ws), _stream(ws.device)))
+    with torch.cuda.device(ws.device):
+        return int(_lib.lib().fkl_get_status(_ptr(ws), _stream(ws.device)))
 
 
 def _raise_on_device_status(ws: torch.Tensor, where: str):
@@ -323,7 +330,8 @@ class FKLLossKeepLogits(torch.autograd.Function):
         dh, dW = ctx.saved_tensors
         g = g.reshape(1).to(torch.float32).contiguous()
         N, d = dh.shape
-        st = _lib.lib().fkl_scale_grads(_ptr(dh), _ptr(dW), N, d, dW.shape[0], _ptr(g), _stream(dh.device))
+        with torch.cuda.device(dh.device):  # the library launches on the current device
+            st = _lib.lib().fkl_scale_grads(_ptr(dh), _ptr(dW), N, d, dW.shape[0], _ptr(g), _stream(dh.device))
         _check(st, "fkl_scale_grads")
         return dh, dW.to(ctx.w_dtype), None, None, None, None, None, None
 
@@ -375,8 +383,9 @@ def selftest_gemm(A: torch.Tensor, B: torch.Tensor, M: int, N: int, K: int, a_mn
     """C = A . B^T on the library's tcgen05 pipeline (see fkl_selftest_gemm)."""
     C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     ws = torch.zeros(256, dtype=torch.uint8, device=A.device)
-    st = _lib.lib().fkl_selftest_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, a_mn, b_mn, bn, _ptr(ws),
-                                      _stream(A.device))
+    with torch.cuda.device(A.device):  # the library launches on the current device
+        st = _lib.lib().fkl_selftest_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, a_mn, b_mn, bn, _ptr(ws),
+                                          _stream(A.device))
     _check(st, "fkl_selftest_gemm")
     s = get_status(ws)
     if s != 0:
