@@ -52,7 +52,7 @@
 //            row's label; dz gains (1 - alpha)/T (q_1 - onehot(label)) per row.
 //   EPI_TMAX each row's kTopPerTile largest logits over the tile, with their
 //            ids (teacher top-K; the first of them is the tile max).
-//   EPI_CAND for the rows flagged by the top-K gather (a tile with kTopPerTile or
+//   EPI_CAND for the rows flagged by topk_rows_kernel (a tile with kTopPerTile or
 //            more logits >= the row's threshold), every logit >= the threshold,
 //            appended to the row's candidate list with an atomic counter; logits
 //            equal to the threshold go to a separate list of at most K ids.  The
