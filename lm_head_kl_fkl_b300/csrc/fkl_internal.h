@@ -33,7 +33,7 @@ enum KernelKind {
     KK_SELFTEST,
     KK_FB_GEMM_LSE_Y,  // tcgen05 GEMM z = h W^T, logsumexp / gather epilogue that also keeps the logits
     KK_FB_DZ,          // dz from the kept logits (elementwise)
-    KK_TK_GEMM_TMAX,   // teacher top-K: tcgen05 GEMM, per-row max of each vocabulary tile
+    KK_TK_GEMM_TMAX,   // teacher top-K: tcgen05 GEMM, per row the eight largest logits of each vocabulary tile
     KK_TK_ROWS,        // teacher top-K: per-row threshold, candidates and selection (one warp per row)
     KK_TK_GEMM_CAND,   // teacher top-K: tcgen05 GEMM again for flagged rows (returns at once if none)
     KK_TK_SELECT,      // teacher top-K: selection for the rows the second tensor-core pass completed
