@@ -487,34 +487,54 @@ void launch_dz_from_logits(void* yz, int64_t pstride, int64_t V, const float* pa
 }
 
 // ---------------------------------------------------------------- h transposed
-// hT[c][r] = h[r][c] over one chunk's rows (row stride of hT: ld elements): the
-// dW GEMM reads h as a K-major operand.  64 x 64 tiles through shared memory,
-// two columns per thread on the loads and two rows per thread on the stores.
-__global__ void transpose_h_kernel(const uint32_t* __restrict__ h, int rows, int d, uint32_t* __restrict__ hT,
-                                   int64_t ld) {
-    __shared__ uint16_t tile[64][66];
+// hT[c][r] = h[r][c] over one chunk's rows (row stride of hT: ld elements, a multiple
+// of 8): the dW GEMM reads h as a K-major operand.  64 x 64 tiles through shared
+// memory with 16-byte global loads and stores (d is a multiple of 8, so a load of
+// eight columns is wholly inside or outside the row).  Rows beyond `rows` are
+// written as zeros up to the next multiple of 8 (inside hT, past the GEMM's map).
+// The tile's rows are 65 elements apart, so that the eight lanes reading one column
+// at rows 8 apart hit eight different banks.
+constexpr int kTrStride = 65;
+
+__global__ void __launch_bounds__(256)
+    transpose_h_kernel(const uint16_t* __restrict__ h, int rows, int d, uint16_t* __restrict__ hT, int64_t ld) {
+    __shared__ uint16_t tile[64 * kTrStride];
     const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
-    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-    for (int i = ty; i < 64; i += 8) {
-        const int r = r0 + i, c = c0 + 2 * tx;
-        uint32_t w = 0;
-        if (r < rows && c < d) w = h[(static_cast<size_t>(r) * d + c) >> 1];
-        tile[i][2 * tx] = static_cast<uint16_t>(w & 0xffffu);
-        tile[i][2 * tx + 1] = static_cast<uint16_t>(w >> 16);
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int q = t + 256 * i;
+        const int row = q >> 3, cc = (q & 7) * 8;  // eight columns of one row
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r0 + row < rows && c0 + cc < d)
+            v = *reinterpret_cast<const uint4*>(h + static_cast<size_t>(r0 + row) * d + c0 + cc);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint16_t* dst = tile + row * kTrStride + cc;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            dst[2 * k] = static_cast<uint16_t>(w[k] & 0xffffu);
+            dst[2 * k + 1] = static_cast<uint16_t>(w[k] >> 16);
+        }
     }
     __syncthreads();
-    for (int i = ty; i < 64; i += 8) {
-        const int c = c0 + i, r = r0 + 2 * tx;
-        if (c < d && r < rows)  // for an odd row count the pair's second half is a zero beyond the map
-            hT[(static_cast<size_t>(c) * ld + r) >> 1] =
-                static_cast<uint32_t>(tile[2 * tx][i]) | (static_cast<uint32_t>(tile[2 * tx + 1][i]) << 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int q = t + 256 * i;
+        const int col = q >> 3, rr = (q & 7) * 8;  // eight rows of one column
+        if (c0 + col >= d || r0 + rr >= rows) continue;
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(tile[(rr + 2 * k) * kTrStride + col]) |
+                   (static_cast<uint32_t>(tile[(rr + 2 * k + 1) * kTrStride + col]) << 16);
+        *reinterpret_cast<uint4*>(hT + static_cast<size_t>(c0 + col) * ld + r0 + rr) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
 void launch_transpose_h(const void* h, int rows, int d, void* hT, int64_t ld, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>((d + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
-    transpose_h_kernel<<<grid, dim3(32, 8), 0, s>>>(static_cast<const uint32_t*>(h), rows, d,
-                                                    static_cast<uint32_t*>(hT), ld);
+    transpose_h_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(h), rows, d, static_cast<uint16_t*>(hT),
+                                            ld);
 }
 
 // ---------------------------------------------------------------- teacher top-K
