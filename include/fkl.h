@@ -77,7 +77,11 @@ typedef enum {
  * It is O(chunk * V + N): one bf16 dz chunk buffer, split-K partials of dh for
  * one chunk, the chunk's h transposed, the sorted teacher cache of one chunk and
  * 4 bytes per token (1.82 GB at N = 131072, d = 2880, V = 201088, K = 100,
- * default chunk). */
+ * default chunk).  The environment variables FKL_BN_DH and FKL_BN_DW (512, 256,
+ * 192 or 128; other values are ignored) override the column-tile width of the dh
+ * and dW GEMMs for tuning sweeps; the dh width sets the split count and so this
+ * size, which is read at each call (a workspace sized under another setting is
+ * refused with FKL_ERR_WORKSPACE if too small). */
 size_t fkl_workspace_size(int64_t N, int d, int64_t V, int K, int chunk);
 
 /* Forward: writes loss (one fp32, device) and lse[N] (fp32, natural-log
