@@ -61,6 +61,9 @@ CASES = [
     # the largest K over many tiles: rows may hold more candidates than the per-row
     # shared-memory list and take the second pass
     (64, 64, 70000, 256),
+    # more than 1024 vocabulary tiles: the per-row kernel keeps 32 tile maxima per lane
+    # in registers and reads the remaining 148 again for each step of its search
+    (64, 64, 300000, 100),
 ]
 
 
