@@ -64,6 +64,9 @@ CASES = [
     # more than 1024 vocabulary tiles: the per-row kernel keeps 32 tile maxima per lane
     # in registers and reads the remaining 148 again for each step of its search
     (64, 64, 300000, 100),
+    # K = 256 over 786 tiles: ~300 candidates above theta per row, sorted in the
+    # per-row kernel's widest register sort (16 slots per lane)
+    (64, 64, 201088, 256),
 ]
 
 
